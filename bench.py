@@ -1,0 +1,376 @@
+"""Benchmark of the 3x3x3 submanifold sparse convolution hot path on B300.
+
+One step = the whole hot path over one synthetic voxel set: coordinate hash
+build + neighbour map (sc_build_map), gather-implicit-GEMM with the fused
+bias (sc_forward).  Inputs are resident in HBM when the timed region starts;
+L2 is flushed (256 MB write) before every timed step.  The printed JSON line
+reports effective TFLOP/s = 2 * pairs * cin * cout / step time (pairs = the
+present (output, neighbour) pairs only) and active voxels/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 3]
+    python bench.py --impl reference ...   # the CPU oracle, on host cores
+
+Multi-GPU: replicas only (each rank runs the same workload on its own GPU,
+no collective on the data path); value = units of all ranks / max time.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse conv3d effective TFLOP/s + active voxels/s (1 B300, % of roofline)"
+FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=0, help="0 = same as --steps (max 500)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("gloo")
+    return dist
+
+
+def max_over_ranks(dist, v):
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([float(v)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % gpu_index)
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle legs (the only places bench.py runs oracle/)
+
+def oracle_sample_run(p, rows, threads=0):
+    """Oracle map build over all voxels + fp64 convolution of `rows`."""
+    import oracle
+    t0 = time.perf_counter()
+    nbr = oracle.build_neighbor_table(p.coords, p.res)
+    oracle.conv(nbr[rows], p.feats, p.weight, p.bias, threads)
+    dt = time.perf_counter() - t0
+    pairs = int((nbr[rows] >= 0).sum())
+    return dt, pairs
+
+
+def cpu_baseline(p, target_s=12.0):
+    """The oracle as it stands on the host cores: map build over all voxels and
+    the fp64 convolution of a row sample sized to ~target_s seconds."""
+    import oracle
+    cin, cout = p.feats.shape[1], p.weight.shape[2]
+    rng = np.random.default_rng(0)
+    t0 = time.perf_counter()
+    nbr = oracle.build_neighbor_table(p.coords, p.res)
+    t_map = time.perf_counter() - t0
+    pilot = rng.choice(p.n, size=min(p.n, 256), replace=False)
+    t0 = time.perf_counter()
+    oracle.conv(nbr[pilot], p.feats, p.weight, p.bias)
+    per_row = max((time.perf_counter() - t0) / len(pilot), 1e-7)
+    m = int(min(p.n, max(256, (target_s - t_map) / per_row)))
+    rows = np.sort(rng.choice(p.n, size=m, replace=False))
+    dt, pairs = oracle_sample_run(p, rows)
+    tflops = 2.0 * pairs * cin * cout / dt / 1e12
+    return {"value": tflops, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": "oracle map build over all %d voxels + fp64 conv of %d sampled output "
+                      "rows (%d pairs) in %.1f s; voxels/s %.3g" % (p.n, m, pairs, dt, m / dt)}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from sparse_voxel_convolution_coord_b300 import synth
+    import oracle
+    p = synth.make_problem(args.config)
+    cin, cout = p.feats.shape[1], p.weight.shape[2]
+    rng = np.random.default_rng(1)
+    # bounded sample per step: the full map build + the conv of 16 output rows
+    samples = [np.sort(rng.choice(p.n, size=16, replace=False)) for _ in range(4)]
+    for i in range(args.warmup):
+        oracle_sample_run(p, samples[i % 4])
+    tot_t, tot_pairs = 0.0, 0
+    for i in range(args.steps):
+        dt, pairs = oracle_sample_run(p, samples[i % 4])
+        tot_t += dt
+        tot_pairs += pairs
+    value = 2.0 * tot_pairs * cin * cout / tot_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": p.config.name, "n_voxels": p.n, "cin": cin, "cout": cout,
+                   "res": p.res},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+                         "kind": "oracle",
+                         "sample": "per step: oracle map build over all %d voxels + fp64 conv "
+                                   "of 16 sampled output rows" % p.n},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    dist = init_dist(world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import sparse_voxel_convolution_coord_b300 as sc
+    from sparse_voxel_convolution_coord_b300 import build_lib, synth
+    build_lib.build()
+    sc.load_library()
+
+    p = synth.make_problem(args.config)
+    cin, cout = p.feats.shape[1], p.weight.shape[2]
+    tdt = torch.bfloat16 if p.config.dtype == "bf16" else torch.float32
+    coords = torch.from_numpy(p.coords).to(dev)
+    feats = torch.from_numpy(p.feats).to(dev).to(tdt)
+    weight = torch.from_numpy(p.weight).to(dev).to(tdt)
+    bias = torch.from_numpy(p.bias).to(dev)
+    out = torch.empty((p.n, cout), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    m = sc.sc_build_map(coords, p.res)
+    pairs = m.pairs
+    m.free()
+    flops = 2.0 * pairs * cin * cout
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        mp = sc.sc_build_map(coords, p.res)
+        if evs is not None:
+            evs[1].record(stream)
+        sc.sc_forward(mp, feats, weight, bias, out)
+        if evs is not None:
+            evs[2].record(stream)
+        mp.free()
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(dist)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize()
+    barrier(dist)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    build_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    fwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    t_step = sum(step_ms) / K
+    t_fwd = sum(fwd_ms) / K
+    t_build = sum(build_ms) / K
+    t_step_max = max_over_ranks(dist, t_step)
+
+    # forward kernel alone (no host gap before its launch): events around back-to-back
+    # forwards on one map, L2 flushed between them
+    mp = sc.sc_build_map(coords, p.res)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(200)]
+    for i in range(200):
+        flush.zero_()
+        kev[i][0].record(stream)
+        sc.sc_forward(mp, feats, weight, bias, out)
+        kev[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_kernel = statistics.median(a.elapsed_time(b) for a, b in kev[20:])
+    mp.free()
+
+    # end to end through the public API from pinned host buffers
+    h_coords = torch.from_numpy(p.coords).pin_memory()
+    h_feats = torch.from_numpy(p.feats).to(tdt).pin_memory()
+    h_weight = torch.from_numpy(p.weight).to(tdt).pin_memory()
+    h_bias = torch.from_numpy(p.bias).pin_memory()
+    h_out = torch.empty((p.n, cout), dtype=torch.float32).pin_memory()
+    d_coords = torch.empty_like(coords)
+    d_feats = torch.empty_like(feats)
+    d_weight = torch.empty_like(weight)
+    d_bias = torch.empty_like(bias)
+    h2d = sum(t.numel() * t.element_size() for t in (h_coords, h_feats, h_weight, h_bias))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        d_coords.copy_(h_coords, non_blocking=True)
+        d_feats.copy_(h_feats, non_blocking=True)
+        d_weight.copy_(h_weight, non_blocking=True)
+        d_bias.copy_(h_bias, non_blocking=True)
+        mp = sc.sc_build_map(d_coords, p.res)
+        sc.sc_forward(mp, d_feats, d_weight, d_bias, out)
+        h_out.copy_(out, non_blocking=True)
+        mp.free()
+
+    KE = args.e2e_steps or min(K, 500)
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    e0.record(stream)
+    for _ in range(KE):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = max_over_ranks(dist, e0.elapsed_time(e1) / KE)
+
+    peaks = load_peaks()
+    achieved = flops / (t_kernel * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": world * flops / (t_step_max * 1e-3) / 1e12,
+        "unit": "TFLOP/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": t_step_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if p.config.dtype == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {"workload": p.config.name, "description": p.config.description,
+                   "n_voxels": p.n, "pairs": pairs, "cin": cin, "cout": cout, "res": p.res,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "flushed before every timed step (256 MB write, outside the step events)"},
+        "voxels_per_s": world * p.n / (t_step_max * 1e-3),
+        "breakdown_ms": {"build_map": t_build, "forward_in_step": t_fwd,
+                         "forward_kernel_alone": t_kernel,
+                         "wall_per_step_incl_flush": wall / K * 1e3},
+        "roofline": {"kernel": "k_conv_tc (gather-implicit-GEMM, tcgen05)", "bound": "tensor",
+                     "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"],
+                     "frac_of_sustained": (achieved / peaks["bf16_tflops_sustained"]
+                                           if peaks.get("bf16_tflops_sustained") else None),
+                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json burst)",
+                     "traffic": None,
+                     "algorithmic_flops_per_launch": flops},
+        "e2e": {"value": world * flops / (t_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": t_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * K,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(p)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

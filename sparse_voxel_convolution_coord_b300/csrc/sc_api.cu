@@ -1,0 +1,323 @@
+// sc_api.cu -- the C ABI declared in include/sc.h.
+//
+// Host-side argument checking, handle lifetime, device allocation and error
+// reporting.  All arithmetic of the method runs in the kernels of sc_map.cu,
+// sc_conv_tc.cu and sc_conv_simt.cu; nothing here computes on the host.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <unordered_set>
+
+#include "sc_internal.cuh"
+
+namespace {
+
+constexpr uint64_t kMagicLive = 0x53434d41504c4956ull;  // "SCMAPLIV"
+
+thread_local sc_status t_status = SC_OK;
+thread_local char t_msg[512] = "";
+
+std::mutex g_mu;
+std::unordered_set<sc_map*>* g_live = nullptr;  // never destroyed (safe at exit)
+
+struct AllocCfg {
+  void* (*alloc)(size_t, void*, void*) = nullptr;
+  void (*free_fn)(void*, void*, void*) = nullptr;
+  void* ctx = nullptr;
+} g_alloc;
+
+sc_status fail(sc_status st, const char* fmt, ...) {
+  t_status = st;
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_msg, sizeof(t_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+sc_status ok() {
+  t_status = SC_OK;
+  t_msg[0] = 0;
+  return SC_OK;
+}
+
+sc_status fail_cuda(cudaError_t e, const char* what) {
+  return fail(SC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool is_live(sc_map* m) {
+  if (!m) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_live && g_live->count(m) && m->magic == kMagicLive;
+}
+
+void* dev_alloc(sc_map* m, size_t bytes, cudaStream_t s) {
+  if (bytes == 0) bytes = 16;
+  if (m->alloc) return m->alloc(bytes, s, m->alloc_ctx);
+  void* p = nullptr;
+  if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return p;
+}
+
+void dev_free(sc_map* m, void* p, cudaStream_t s) {
+  if (!p) return;
+  if (m->free_fn)
+    m->free_fn(p, s, m->alloc_ctx);
+  else
+    cudaFreeAsync(p, s);
+}
+
+void release_buffers(sc_map* m, cudaStream_t s) {
+  dev_free(m, m->hash.slots, s);
+  dev_free(m, m->nbr, s);
+  dev_free(m, m->tile_mask, s);
+  dev_free(m, m->d_status, s);
+  m->hash.slots = nullptr;
+  m->nbr = nullptr;
+  m->tile_mask = nullptr;
+  m->d_status = nullptr;
+  m->d_pairs = nullptr;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int bit_length(uint64_t v) { return v ? 64 - __builtin_clzll(v) : 0; }
+
+}  // namespace
+
+extern "C" {
+
+sc_status sc_last_error(void) { return t_status; }
+const char* sc_last_error_msg(void) { return t_msg; }
+const char* sc_version(void) { return "sc-b300 0.1 (sm_103a)"; }
+
+sc_status sc_set_allocator(void* (*alloc)(size_t, void*, void*),
+                           void (*free_fn)(void*, void*, void*), void* ctx) {
+  if ((alloc == nullptr) != (free_fn == nullptr))
+    return fail(SC_ERR_INVALID_ARG, "sc_set_allocator: alloc and free must both be set or NULL");
+  g_alloc.alloc = alloc;
+  g_alloc.free_fn = free_fn;
+  g_alloc.ctx = ctx;
+  return ok();
+}
+
+sc_handle sc_build_map(const int32_t* coords, int64_t n, int32_t res, void* stream) {
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (n < 0 || n >= (int64_t(1) << 31)) {
+    fail(SC_ERR_INVALID_ARG, "sc_build_map: n=%lld outside [0, 2^31)", (long long)n);
+    return nullptr;
+  }
+  if (res < 1 || res > (1 << 20)) {
+    fail(SC_ERR_INVALID_ARG, "sc_build_map: res=%d outside [1, 2^20]", res);
+    return nullptr;
+  }
+  if (n > 0 && (coords == nullptr || !aligned(coords, 16))) {
+    fail(SC_ERR_INVALID_ARG, "sc_build_map: coords must be a 16-byte aligned device pointer");
+    return nullptr;
+  }
+  sc_map* m = new sc_map();
+  std::memset(m, 0, sizeof(*m));
+  m->magic = kMagicLive;
+  cudaGetDevice(&m->device);
+  m->n = n;
+  m->res = res;
+  m->alloc = g_alloc.alloc;
+  m->free_fn = g_alloc.free_fn;
+  m->alloc_ctx = g_alloc.ctx;
+  m->ntiles = (n + sc::kTileRows - 1) / sc::kTileRows;
+
+  if (n > 0) {
+    const int vbits = bit_length((uint64_t)n);
+    const int kbits = 64 - vbits;
+    const uint64_t res3 = (uint64_t)res * res * res;
+    const uint64_t kspace = (kbits >= 64) ? ~0ull : (1ull << kbits);
+    const uint64_t bmax = kspace / res3;
+    if (bmax == 0) {
+      delete m;
+      fail(SC_ERR_UNSUPPORTED, "sc_build_map: res^3 exceeds the 2^%d key space for n=%lld", kbits,
+           (long long)n);
+      return nullptr;
+    }
+    uint64_t cap = 64;
+    int log2cap = 6;
+    while (cap < 2ull * (uint64_t)n) {
+      cap <<= 1;
+      ++log2cap;
+    }
+    m->hash.cap_mask = cap - 1;
+    m->hash.log2cap = log2cap;
+    m->hash.vbits = vbits;
+    m->hash.res = res;
+    m->hash.bmax = bmax;
+    m->hash.n = n;
+    m->hash.slots = static_cast<uint64_t*>(dev_alloc(m, cap * sizeof(uint64_t), s));
+    m->nbr = static_cast<int32_t*>(dev_alloc(m, (size_t)n * sc::kTaps * sizeof(int32_t), s));
+    m->tile_mask = static_cast<uint32_t*>(dev_alloc(m, (size_t)m->ntiles * sizeof(uint32_t), s));
+    m->d_status = static_cast<uint32_t*>(dev_alloc(m, 16, s));
+    if (!m->hash.slots || !m->nbr || !m->tile_mask || !m->d_status) {
+      release_buffers(m, s);
+      delete m;
+      fail(SC_ERR_ALLOC, "sc_build_map: device allocation failed (n=%lld)", (long long)n);
+      return nullptr;
+    }
+    m->d_pairs = reinterpret_cast<unsigned long long*>(m->d_status + 2);
+    cudaError_t e = cudaMemsetAsync(m->hash.slots, 0xFF, cap * sizeof(uint64_t), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(m->d_status, 0, 16, s);
+    if (e == cudaSuccess) e = sc::launch_hash_insert(coords, m->hash, m->d_status, s);
+    if (e == cudaSuccess)
+      e = sc::launch_neighbor_query(coords, m->hash, m->nbr, m->tile_mask, m->d_pairs,
+                                    m->d_status, s);
+    uint32_t host[4] = {0, 0, 0, 0};
+    if (e == cudaSuccess) e = cudaMemcpyAsync(host, m->d_status, 16, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+      release_buffers(m, s);
+      delete m;
+      fail_cuda(e, "sc_build_map");
+      return nullptr;
+    }
+    const uint32_t st = host[0];
+    if (st) {
+      release_buffers(m, s);
+      delete m;
+      if (st & sc::kStatRange)
+        fail(SC_ERR_COORD_RANGE,
+             "sc_build_map: a coordinate lies outside [0,%d)^3 or has a negative batch index",
+             res);
+      else if (st & sc::kStatKeySpace)
+        fail(SC_ERR_UNSUPPORTED,
+             "sc_build_map: batch index >= %llu does not fit the hash key for res=%d, n=%lld",
+             (unsigned long long)bmax, res, (long long)n);
+      else if (st & sc::kStatDuplicate)
+        fail(SC_ERR_DUPLICATE, "sc_build_map: duplicate (batch,x,y,z) rows");
+      else
+        fail(SC_ERR_TABLE_FULL, "sc_build_map: hash probe bound exceeded");
+      return nullptr;
+    }
+    uint64_t pairs;
+    std::memcpy(&pairs, host + 2, sizeof(pairs));
+    m->npairs = (int64_t)pairs;
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_live) g_live = new std::unordered_set<sc_map*>();
+    g_live->insert(m);
+  }
+  ok();
+  return m;
+}
+
+sc_status sc_free_map(sc_handle h, void* stream) {
+  if (h == nullptr) return ok();
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_live || !g_live->count(h) || h->magic != kMagicLive)
+      return fail(SC_ERR_BAD_HANDLE, "sc_free_map: handle is not live");
+    g_live->erase(h);
+  }
+  release_buffers(h, static_cast<cudaStream_t>(stream));
+  h->magic = 0;
+  delete h;
+  return ok();
+}
+
+int64_t sc_map_size(sc_handle h) {
+  if (!is_live(h)) {
+    fail(SC_ERR_BAD_HANDLE, "sc_map_size: handle is not live");
+    return -1;
+  }
+  ok();
+  return h->n;
+}
+
+int64_t sc_map_pairs(sc_handle h) {
+  if (!is_live(h)) {
+    fail(SC_ERR_BAD_HANDLE, "sc_map_pairs: handle is not live");
+    return -1;
+  }
+  ok();
+  return h->npairs;
+}
+
+sc_status sc_get_neighbor_table(sc_handle h, int32_t* nbr_out, void* stream) {
+  if (!is_live(h)) return fail(SC_ERR_BAD_HANDLE, "sc_get_neighbor_table: handle is not live");
+  if (h->n == 0) return ok();
+  if (!nbr_out) return fail(SC_ERR_INVALID_ARG, "sc_get_neighbor_table: nbr_out is NULL");
+  cudaError_t e = cudaMemcpyAsync(nbr_out, h->nbr, (size_t)h->n * sc::kTaps * sizeof(int32_t),
+                                  cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "sc_get_neighbor_table");
+  return ok();
+}
+
+sc_status sc_get_pairs(sc_handle h, int64_t* off_host, int32_t* in, int32_t* out, void* stream) {
+  if (!is_live(h)) return fail(SC_ERR_BAD_HANDLE, "sc_get_pairs: handle is not live");
+  if (!off_host) return fail(SC_ERR_INVALID_ARG, "sc_get_pairs: off_host is NULL");
+  if (h->n == 0) {
+    for (int k = 0; k < 28; ++k) off_host[k] = 0;
+    return ok();
+  }
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* scratch = dev_alloc(h, sc::pairs_scratch_bytes(h->n), s);
+  if (!scratch) return fail(SC_ERR_ALLOC, "sc_get_pairs: scratch allocation failed");
+  cudaError_t e = sc::launch_pairs(h, off_host, in, out, scratch, s);
+  dev_free(h, scratch, s);
+  if (e != cudaSuccess) return fail_cuda(e, "sc_get_pairs");
+  return ok();
+}
+
+sc_status sc_forward(sc_handle h, const void* feats, const void* weight, const float* bias,
+                     float* out, int32_t cin, int32_t cout, sc_dtype dtype, void* stream) {
+  if (!is_live(h)) return fail(SC_ERR_BAD_HANDLE, "sc_forward: handle is not live");
+  if (cin < 1 || cout < 1) return fail(SC_ERR_INVALID_ARG, "sc_forward: cin/cout must be >= 1");
+  if (dtype != SC_F32 && dtype != SC_BF16)
+    return fail(SC_ERR_UNSUPPORTED, "sc_forward: dtype %d not supported", (int)dtype);
+  if (dtype == SC_BF16 && !sc::conv_tc_supported(cin, cout))
+    return fail(SC_ERR_UNSUPPORTED,
+                "sc_forward: bf16 needs cin in {16,32} or a multiple of 64 <= 1024 and cout a "
+                "multiple of 16 <= 256 (got cin=%d cout=%d)",
+                cin, cout);
+  if (dtype == SC_F32 && cout > 256)
+    return fail(SC_ERR_UNSUPPORTED, "sc_forward: fp32 path supports cout <= 256 (got %d)", cout);
+  if (h->n == 0) return ok();
+  if (!feats || !weight || !out)
+    return fail(SC_ERR_INVALID_ARG, "sc_forward: feats, weight and out must be non-NULL");
+  if (!aligned(feats, 16) || !aligned(weight, 16) || !aligned(out, 16) ||
+      (bias && !aligned(bias, 4)))
+    return fail(SC_ERR_INVALID_ARG, "sc_forward: feats/weight/out must be 16-byte aligned");
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != h->device)
+    return fail(SC_ERR_INVALID_ARG, "sc_forward: map lives on device %d, current is %d",
+                h->device, dev);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (dtype == SC_BF16)
+    e = sc::launch_conv_tc_bf16(h, feats, weight, bias, out, cin, cout, s);
+  else
+    e = sc::launch_conv_simt_f32(h, static_cast<const float*>(feats),
+                                 static_cast<const float*>(weight), bias, out, cin, cout, s);
+  if (e != cudaSuccess) return fail_cuda(e, "sc_forward");
+  return ok();
+}
+
+sc_status sc_device_status(sc_handle h, void* stream) {
+  if (!is_live(h)) return fail(SC_ERR_BAD_HANDLE, "sc_device_status: handle is not live");
+  if (h->n == 0) return ok();
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t st = 0;
+  cudaError_t e = cudaMemcpyAsync(&st, h->d_status, 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->d_status, 0, 4, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(e, "sc_device_status");
+  if (st & sc::kStatTimeout)
+    return fail(SC_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (device status 0x%x)", st);
+  if (st & sc::kStatTableFull) return fail(SC_ERR_TABLE_FULL, "hash probe bound exceeded");
+  if (st) return fail(SC_ERR_CUDA, "device status 0x%x", st);
+  return ok();
+}
+
+}  // extern "C"

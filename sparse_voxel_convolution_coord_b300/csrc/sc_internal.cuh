@@ -1,0 +1,255 @@
+// sc_internal.cuh -- shared definitions of the sm_103a sparse-conv library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sc.h"
+
+namespace sc {
+
+// Rows per output tile: one tcgen05 accumulator tile (M = 128, one TMEM lane
+// per row) and one CTA of the neighbour-query kernel.
+constexpr int kTileRows = 128;
+constexpr int kTaps = 27;
+constexpr int kCentre = 13;
+constexpr uint64_t kEmptySlot = ~0ull;
+
+// Device status word bits (the map's `d_status`).
+enum : uint32_t {
+  kStatRange = 1u,
+  kStatDuplicate = 2u,
+  kStatTableFull = 4u,
+  kStatTimeout = 8u,
+  kStatKeySpace = 16u,  // (batch+1) * res^3 does not fit the packed key field
+};
+
+// ---------------------------------------------------------------------------
+// Coordinate hash: packed 64-bit slots (key << vbits | row), empty = all ones.
+// key = ((b * res + x) * res + y) * res + z; vbits = bit length of n, so a
+// row index never fills its field and a live slot is never all ones.
+
+struct HashParams {
+  uint64_t* slots;
+  uint64_t cap_mask;   // capacity - 1 (capacity a power of two)
+  int log2cap;
+  int vbits;
+  int res;
+  uint64_t bmax;       // batch indices must be < bmax
+  int64_t n;
+};
+
+__device__ __forceinline__ uint64_t hash_home(uint64_t key, int log2cap) {
+  // Fibonacci hashing: the top log2cap bits of key * 2^64/phi.
+  return (key * 0x9E3779B97F4A7C15ull) >> (64 - log2cap);
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier / TMA / tcgen05 wrappers (inline PTX, sm_100+ family).
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: returns false if the phase did not complete within ~2 s or
+// another role of the CTA has already given up (*abort != 0).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 255u) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > 2000000000ull) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Four rows r0..r3 (each one box of the 2-D map, box height 1) at column x.
+// Rows outside the tensor are filled with zeros and still count in bytes.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int4 rows) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(rows.x), "r"(rows.y), "r"(rows.z), "r"(rows.w), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// TMEM allocation (whole warp), address written to shared memory.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc], bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 op issued so far by this thread is done.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns: thread t gets row (lane base + t).
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 layout, version 1).
+//   layout: 0 none, 2 = 128B swizzle, 4 = 64B swizzle, 6 = 32B swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes,
+                                              uint32_t sbo_bytes, uint32_t layout) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version for sm_100 family
+  d |= (uint64_t)(layout & 7u) << 61;
+  return d;
+}
+
+// Instruction descriptor: kind::f16, A = B = bf16, D = fp32, A K-major,
+// B MN-major (row-major W[k][ci][co] has co contiguous), shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
+  return (1u << 4)                      // D format fp32
+         | (1u << 7)                    // A format bf16
+         | (1u << 10)                   // B format bf16
+         | (0u << 15)                   // A K-major
+         | (1u << 16)                   // B MN-major
+         | ((uint32_t)(n >> 3) << 17)   // N / 8
+         | ((uint32_t)(m >> 4) << 24);  // M / 16
+}
+
+}  // namespace sc
+
+// ---------------------------------------------------------------------------
+// Host-side launch entry points implemented in the kernel files.
+
+struct sc_map {
+  uint64_t magic;
+  int device;
+  int64_t n;
+  int32_t res;
+  int64_t ntiles;
+  int64_t npairs;
+  sc::HashParams hash;
+  int32_t* nbr;          // [n][27]
+  uint32_t* tile_mask;   // [ntiles] OR of the 27-bit presence masks of a tile's rows
+  uint32_t* d_status;    // device status word + pair counter scratch
+  unsigned long long* d_pairs;
+  void* (*alloc)(size_t, void*, void*);
+  void (*free_fn)(void*, void*, void*);
+  void* alloc_ctx;
+};
+
+namespace sc {
+
+cudaError_t launch_hash_insert(const int32_t* coords, const HashParams& hp, uint32_t* status,
+                               cudaStream_t s);
+cudaError_t launch_neighbor_query(const int32_t* coords, const HashParams& hp, int32_t* nbr,
+                                  uint32_t* tile_mask, unsigned long long* pair_count,
+                                  uint32_t* status, cudaStream_t s);
+cudaError_t launch_pairs(const sc_map* m, int64_t* off_host, int32_t* in, int32_t* out,
+                         void* scratch, cudaStream_t s);
+size_t pairs_scratch_bytes(int64_t n);
+cudaError_t launch_conv_simt_f32(const sc_map* m, const float* feats, const float* w,
+                                 const float* bias, float* out, int cin, int cout,
+                                 cudaStream_t s);
+// Returns cudaErrorNotSupported for shapes outside the tensor-core envelope.
+cudaError_t launch_conv_tc_bf16(const sc_map* m, const void* feats, const void* w,
+                                const float* bias, float* out, int cin, int cout,
+                                cudaStream_t s);
+bool conv_tc_supported(int cin, int cout);
+
+}  // namespace sc

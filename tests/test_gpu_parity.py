@@ -1,0 +1,300 @@
+"""GPU parity: the CUDA library against the CPU oracle, through the C ABI.
+
+Maps (neighbour table, pair lists) must match bit for bit.  Convolution
+outputs must meet the bars of the method's acceptance criteria: fp32 inputs
+relative L2 <= 1e-5; bf16 inputs relative L2 <= 2e-3 and max |err| <=
+1e-2 * rms(ref), against the oracle fed the same bf16-rounded values.
+relative L2 = ||gpu - ref||_2 / ||ref||_2 over the compared outputs,
+rms(ref) = ||ref||_2 / sqrt(count).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from sparse_voxel_convolution_coord_b300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+F32_REL_L2 = 1e-5
+BF16_REL_L2 = 2e-3
+BF16_MAX_ABS_OVER_RMS = 1e-2
+
+
+@pytest.fixture(scope="module")
+def sc():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sparse_voxel_convolution_coord_b300 as m
+    from sparse_voxel_convolution_coord_b300 import build_lib
+    build_lib.build()
+    m.load_library()
+    return m
+
+
+def to_dev(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    return t.to(dtype) if dtype is not None else t
+
+
+def gpu_map(sc, coords, res):
+    m = sc.sc_build_map(to_dev(coords.astype(np.int32)), res)
+    nbr = sc.sc_get_neighbor_table(m).cpu().numpy()
+    return m, nbr
+
+
+def gpu_conv(sc, m, feats, weight, bias, dtype):
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    out = sc.sc_forward(m, to_dev(feats, tdt), to_dev(weight, tdt),
+                        None if bias is None else to_dev(bias))
+    sc.sc_device_status(m)
+    return out.cpu().numpy().astype(np.float64)
+
+
+def assert_close(got, ref, dtype, what=""):
+    err = got - ref
+    nref = np.linalg.norm(ref)
+    rel = np.linalg.norm(err) / max(nref, 1e-300)
+    if dtype == "f32":
+        assert rel <= F32_REL_L2, "%s rel L2 %.3e > %.0e" % (what, rel, F32_REL_L2)
+    else:
+        rms = nref / np.sqrt(ref.size)
+        mx = np.abs(err).max() if err.size else 0.0
+        assert rel <= BF16_REL_L2, "%s rel L2 %.3e" % (what, rel)
+        assert mx <= BF16_MAX_ABS_OVER_RMS * rms, "%s max abs %.3e > 1e-2 rms %.3e" % (what, mx, rms)
+    return rel
+
+
+def random_coords(rng, nbatch, res, density, batch_ids=None):
+    rows = []
+    ids = batch_ids if batch_ids is not None else range(nbatch)
+    for b in ids:
+        occ = rng.random((res, res, res)) < density
+        xyz = np.argwhere(occ)
+        rows.append(np.concatenate([np.full((len(xyz), 1), b), xyz], axis=1))
+    return np.concatenate(rows).astype(np.int32)
+
+
+# ---------------------------------------------------------------------------
+# maps
+
+@pytest.mark.parametrize("key", [1, 2, 3, 4, 5])
+def test_map_bit_exact_configs(sc, key):
+    p = synth.make_problem(key)
+    m, nbr = gpu_map(sc, p.coords, p.res)
+    want = oracle.build_neighbor_table(p.coords, p.res)
+    np.testing.assert_array_equal(nbr, want)
+    assert sc.sc_map_pairs(m) == int((want >= 0).sum())
+    off, pin, pout = sc.sc_get_pairs(m)
+    woff, wpin, wpout = oracle.pairs(want)
+    np.testing.assert_array_equal(off.numpy(), woff)
+    np.testing.assert_array_equal(pin.cpu().numpy(), wpin)
+    np.testing.assert_array_equal(pout.cpu().numpy(), wpout)
+    m.free()
+
+
+def test_map_shuffled_and_repeatable(sc):
+    p = synth.make_problem(3)
+    rng = np.random.default_rng(1)
+    perm = rng.permutation(p.n)
+    c = p.coords[perm]
+    m1, nbr1 = gpu_map(sc, c, p.res)
+    m2, nbr2 = gpu_map(sc, c, p.res)
+    np.testing.assert_array_equal(nbr1, nbr2)
+    np.testing.assert_array_equal(nbr1, oracle.build_neighbor_table(c, p.res))
+    m1.free()
+    m2.free()
+
+
+@pytest.mark.parametrize("case", ["full_cube", "res1_batches", "batch_gaps", "single",
+                                  "line_z", "sparse_big_res"])
+def test_map_edge_cases(sc, case):
+    rng = np.random.default_rng(2)
+    if case == "full_cube":
+        L = 9
+        xyz = np.argwhere(np.ones((L, L, L), bool))
+        coords, res = np.concatenate([np.zeros((len(xyz), 1)), xyz], 1).astype(np.int32), L
+    elif case == "res1_batches":
+        coords, res = np.array([[b, 0, 0, 0] for b in range(5)], np.int32), 1
+    elif case == "batch_gaps":
+        coords, res = random_coords(rng, 0, 12, 0.2, batch_ids=[0, 3, 7]), 12
+    elif case == "single":
+        coords, res = np.array([[2, 5, 0, 7]], np.int32), 8
+    elif case == "line_z":
+        coords, res = np.array([[0, 3, 3, z] for z in range(300)], np.int32), 300
+    else:
+        coords, res = random_coords(rng, 1, 64, 0.002), 1 << 14
+        coords[:, 1:] *= 200
+    m, nbr = gpu_map(sc, coords, res)
+    want = oracle.build_neighbor_table(coords, res)
+    np.testing.assert_array_equal(nbr, want)
+    if case == "full_cube":
+        assert sc.sc_map_pairs(m) == (3 * 9 - 2) ** 3
+    m.free()
+
+
+def test_map_empty(sc):
+    m = sc.sc_build_map(torch.zeros((0, 4), dtype=torch.int32, device="cuda"), 16)
+    assert sc.sc_map_size(m) == 0 and sc.sc_map_pairs(m) == 0
+    off, pin, pout = sc.sc_get_pairs(m)
+    assert off.abs().sum() == 0 and pin.numel() == 0
+    out = sc.sc_forward(m, torch.zeros((0, 32), dtype=torch.bfloat16, device="cuda"),
+                        torch.zeros((27, 32, 32), dtype=torch.bfloat16, device="cuda"))
+    assert out.shape == (0, 32)
+    m.free()
+
+
+@pytest.mark.parametrize("coords,res,code", [
+    ([[0, 0, 0, 8]], 8, 2),                       # x/y/z == res
+    ([[0, 0, -1, 0]], 8, 2),                      # negative coordinate
+    ([[-1, 0, 0, 0]], 8, 2),                      # negative batch
+    ([[0, 1, 2, 3], [0, 1, 2, 3]], 8, 3),         # duplicate
+    ([[0, 1, 2, 3], [0, 1, 2, 3], [0, 9, 0, 0]], 8, 2),  # range wins over duplicate
+])
+def test_map_errors(sc, coords, res, code):
+    with pytest.raises(sc.ScError) as e:
+        sc.sc_build_map(to_dev(np.array(coords, np.int32)), res)
+    assert e.value.code == code
+    # the oracle agrees on the class of error
+    with pytest.raises(oracle.OracleError) as eo:
+        oracle.build_neighbor_table(np.array(coords, np.int32), res)
+    assert eo.value.code == {2: oracle.COORD_RANGE, 3: oracle.DUPLICATE}[code]
+
+
+def test_key_space_overflow_is_unsupported(sc):
+    # n = 1 leaves 63 key bits; res = 2^14 uses 42 of them, so batch < 2^21.
+    with pytest.raises(sc.ScError) as e:
+        sc.sc_build_map(to_dev(np.array([[1 << 22, 0, 0, 0]], np.int32)), 1 << 14)
+    assert e.value.code == sc.SC_ERR_UNSUPPORTED
+    m = sc.sc_build_map(to_dev(np.array([[(1 << 21) - 1, 5, 5, 5]], np.int32)), 1 << 14)
+    m.free()
+
+
+def test_double_free_is_caught(sc):
+    m = sc.sc_build_map(to_dev(np.array([[0, 1, 1, 1]], np.int32)), 4)
+    ptr = m.ptr
+    m.free()
+    import ctypes
+    assert sc.load_library().sc_free_map(ctypes.c_void_p(ptr), None) == sc.SC_ERR_BAD_HANDLE
+
+
+# ---------------------------------------------------------------------------
+# convolution
+
+def check_problem(sc, coords, res, feats, weight, bias, dtype, rows=None, what=""):
+    m, nbr = gpu_map(sc, coords, res)
+    got = gpu_conv(sc, m, feats, weight, bias, dtype)
+    if rows is None:
+        ref = oracle.conv(nbr, feats, weight, bias)
+        rel = assert_close(got, ref, dtype, what)
+    else:
+        ref = oracle.conv(nbr[rows], feats, weight, bias)
+        rel = assert_close(got[rows], ref, dtype, what)
+    m.free()
+    return rel
+
+
+@pytest.mark.parametrize("key", [1, 2, 5])
+def test_conv_configs_full(sc, key):
+    p = synth.make_problem(key)
+    check_problem(sc, p.coords, p.res, p.feats, p.weight, p.bias, p.config.dtype,
+                  what="config %d" % key)
+
+
+@pytest.mark.parametrize("key", [3, 4])
+def test_conv_configs_sampled(sc, key):
+    p = synth.make_problem(key)
+    rng = np.random.default_rng(10 + key)
+    n = p.n
+    rows = np.unique(np.concatenate([np.arange(0, 256), np.arange(n - 300, n),
+                                     rng.choice(n, size=3000, replace=False)]))
+    check_problem(sc, p.coords, p.res, p.feats, p.weight, p.bias, p.config.dtype, rows=rows,
+                  what="config %d" % key)
+
+
+SHAPES = [(16, 16), (32, 48), (64, 64), (64, 192), (128, 32), (192, 256), (256, 256),
+          (1024, 16), (32, 256)]
+
+
+@pytest.mark.parametrize("cin,cout", SHAPES)
+def test_conv_bf16_shapes(sc, cin, cout):
+    rng = np.random.default_rng(cin * 1000 + cout)
+    coords = random_coords(rng, 2, 14, 0.25)          # ~1370 rows: 11 tiles, ragged tail
+    feats, weight, bias = synth.make_tensors(len(coords), cin, cout, "bf16", cin + cout)
+    check_problem(sc, coords, 14, feats, weight, bias, "bf16", what="%dx%d" % (cin, cout))
+
+
+@pytest.mark.parametrize("cin,cout", [(32, 32), (3, 5), (100, 256), (64, 128)])
+def test_conv_f32_shapes(sc, cin, cout):
+    rng = np.random.default_rng(cin + 7 * cout)
+    coords = random_coords(rng, 2, 12, 0.3)
+    feats, weight, bias = synth.make_tensors(len(coords), cin, cout, "f32", cin)
+    check_problem(sc, coords, 12, feats, weight, bias, "f32", what="f32 %dx%d" % (cin, cout))
+
+
+@pytest.mark.parametrize("dtype,c", [("bf16", 64), ("f32", 32), ("bf16", 32)])
+def test_identity_centre_tap_is_exact(sc, dtype, c):
+    p = synth.make_problem(2)
+    feats = p.feats[:, :c] if dtype == "bf16" else p.feats[:, :c].copy()
+    w = np.zeros((27, c, c), np.float32)
+    w[13] = np.eye(c)
+    m, _ = gpu_map(sc, p.coords, p.res)
+    got = gpu_conv(sc, m, feats, w, None, dtype)
+    np.testing.assert_array_equal(got, feats.astype(np.float64))
+    m.free()
+
+
+def test_isolated_voxels(sc):
+    coords = np.array([[0, 1, 1, 1], [0, 5, 5, 5], [1, 1, 1, 1], [3, 0, 0, 0]], np.int32)
+    feats, weight, bias = synth.make_tensors(4, 64, 64, "bf16", 77)
+    m, nbr = gpu_map(sc, coords, 8)
+    assert (nbr >= 0).sum() == 4
+    got = gpu_conv(sc, m, feats, weight, bias, "bf16")
+    want = feats.astype(np.float64) @ weight[13].astype(np.float64) + bias
+    assert_close(got, want, "bf16")
+    m.free()
+
+
+def test_permutation_equivariance(sc):
+    p = synth.make_problem(2)
+    m, _ = gpu_map(sc, p.coords, p.res)
+    base = gpu_conv(sc, m, p.feats, p.weight, p.bias, "bf16")
+    m.free()
+    perm = np.random.default_rng(3).permutation(p.n)
+    m, _ = gpu_map(sc, p.coords[perm], p.res)
+    got = gpu_conv(sc, m, p.feats[perm], p.weight, p.bias, "bf16")
+    assert_close(got, base[perm], "bf16")
+    m.free()
+
+
+def test_forward_deterministic(sc):
+    p = synth.make_problem(3)
+    m, _ = gpu_map(sc, p.coords, p.res)
+    a = gpu_conv(sc, m, p.feats, p.weight, p.bias, "bf16")
+    b = gpu_conv(sc, m, p.feats, p.weight, p.bias, "bf16")
+    np.testing.assert_array_equal(a, b)
+    m.free()
+
+
+def test_forward_rejects_bad_arguments(sc):
+    import ctypes
+    p = synth.make_problem(2)
+    m, _ = gpu_map(sc, p.coords, p.res)
+    lib = sc.load_library()
+    f = to_dev(p.feats, torch.bfloat16)
+    w = to_dev(p.weight, torch.bfloat16)
+    out = torch.empty((p.n, 64), device="cuda")
+    P = ctypes.c_void_p
+    # unaligned feats
+    assert lib.sc_forward(P(m.ptr), P(f.data_ptr() + 2), P(w.data_ptr()), None,
+                          P(out.data_ptr()), 64, 64, 1, None) == sc.SC_ERR_INVALID_ARG
+    # unsupported shapes
+    assert lib.sc_forward(P(m.ptr), P(f.data_ptr()), P(w.data_ptr()), None,
+                          P(out.data_ptr()), 48, 64, 1, None) == sc.SC_ERR_UNSUPPORTED
+    assert lib.sc_forward(P(m.ptr), P(f.data_ptr()), P(w.data_ptr()), None,
+                          P(out.data_ptr()), 64, 72, 1, None) == sc.SC_ERR_UNSUPPORTED
+    assert lib.sc_forward(P(m.ptr), P(f.data_ptr()), P(w.data_ptr()), None,
+                          P(out.data_ptr()), 64, 64, 7, None) == sc.SC_ERR_UNSUPPORTED
+    assert lib.sc_forward(P(m.ptr), None, P(w.data_ptr()), None,
+                          P(out.data_ptr()), 64, 64, 1, None) == sc.SC_ERR_INVALID_ARG
+    m.free()
