@@ -163,6 +163,37 @@ SC_API sc_status sc_set_allocator(void* (*alloc)(size_t bytes, void* stream, voi
  */
 SC_API sc_status sc_device_status(sc_handle h, void* stream);
 
+/*
+ * Neighbour table without any device allocation.  The pages have no
+ * counterpart to this call; it exists for callers that cannot let a library
+ * allocate device memory: runtimes that give a plugin a fixed memory budget
+ * and forbid allocation while work is enqueued, loops where the implicit
+ * device synchronisation of cudaMalloc is unacceptable, and deployments that
+ * reserve all device memory up front.
+ *
+ * It writes the same table as sc_build_map + sc_get_neighbor_table:
+ *   coords     device int32 [n][4] (batch, x, y, z), 16-byte aligned.
+ *   n          0 <= n <= 524288 (2^19); larger n gives SC_ERR_UNSUPPORTED.
+ *   res        grid side, 1 <= res <= 2^20 (same key-space rule as sc_build_map).
+ *   nbr_out    device int32 [n][27], 16-byte aligned, owned by the caller.
+ *   pairs_out  host int64, receives the pair count P; may be NULL.
+ * Errors as sc_build_map (SC_ERR_COORD_RANGE, SC_ERR_DUPLICATE, ...).
+ * Synchronises `stream` once, to read the status and pair count.
+ *
+ * Scratch: the hash table (2^20 slots, 8 MiB) and 16 KiB of tile masks and
+ * status words live in one static device array that every device which loads
+ * the library holds until the process exits.  The first call on a device
+ * looks up that array's device address (cudaGetSymbolAddress); make that
+ * first call before any stream capture.  All calls share the one array and
+ * each clears what it needs, so calls that overlap on the GPU (other streams,
+ * other host threads) race and must be serialised by the caller.  The call
+ * itself allocates nothing: no cudaMalloc, cudaFree or allocating library
+ * routine.
+ */
+SC_API sc_status sc_build_neighbor_table_noalloc(const int32_t* coords, int64_t n, int32_t res,
+                                                 int32_t* nbr_out, int64_t* pairs_out,
+                                                 void* stream);
+
 /* Thread-local status and message of the last failing call on this thread. */
 SC_API sc_status sc_last_error(void);
 SC_API const char* sc_last_error_msg(void);

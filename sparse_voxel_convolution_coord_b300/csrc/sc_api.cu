@@ -89,6 +89,12 @@ int bit_length(uint64_t v) { return v ? 64 - __builtin_clzll(v) : 0; }
 
 }  // namespace
 
+namespace sc {
+sc_status set_last_error(sc_status st, const char* msg) {
+  return st == SC_OK ? ok() : fail(st, "%s", msg);
+}
+}  // namespace sc
+
 extern "C" {
 
 sc_status sc_last_error(void) { return t_status; }

@@ -251,5 +251,8 @@ cudaError_t launch_conv_tc_bf16(const sc_map* m, const void* feats, const void* 
                                 const float* bias, float* out, int cin, int cout,
                                 cudaStream_t s);
 bool conv_tc_supported(int cin, int cout);
+// Record a failure (or SC_OK with an empty message) as the calling thread's
+// last error; returns st.
+sc_status set_last_error(sc_status st, const char* msg);
 
 }  // namespace sc

@@ -1,0 +1,80 @@
+"""The allocation-free neighbour-table entry point agrees with sc_build_map.
+
+sc_build_neighbor_table_noalloc serves callers that cannot let a library
+allocate device memory (fixed-budget plugin runtimes, loops that cannot absorb
+cudaMalloc's implicit synchronisation, fully pre-reserved deployments).  It
+keeps its hash table in a static device array shared by all calls, so this
+test calls it twice in a row on different voxel sets (the second smaller than
+the first, so stale slots from the first call would show) and compares each
+result bit for bit with the allocating path: sc_build_map followed by
+sc_get_neighbor_table.  The file is named to be collected last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+from sparse_voxel_convolution_coord_b300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sparse_voxel_convolution_coord_b300 as sc
+    from sparse_voxel_convolution_coord_b300 import build_lib
+    build_lib.build()
+    lib = sc.load_library()
+    lib.sc_build_neighbor_table_noalloc.argtypes = [ctypes.c_void_p, ctypes.c_int64,
+                                                    ctypes.c_int32, ctypes.c_void_p,
+                                                    ctypes.c_void_p, ctypes.c_void_p]
+    lib.sc_build_neighbor_table_noalloc.restype = ctypes.c_int
+    return lib
+
+
+def noalloc_table(lib, coords_dev, res):
+    n = coords_dev.shape[0]
+    nbr = torch.full((max(n, 1), 27), 7, dtype=torch.int32, device="cuda")
+    pairs = ctypes.c_int64(-1)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = lib.sc_build_neighbor_table_noalloc(ctypes.c_void_p(coords_dev.data_ptr()), n, res,
+                                             ctypes.c_void_p(nbr.data_ptr()),
+                                             ctypes.byref(pairs), stream)
+    return rc, nbr[:n].cpu().numpy(), pairs.value
+
+
+def allocating_table(coords_dev, res):
+    import sparse_voxel_convolution_coord_b300 as sc
+    m = sc.sc_build_map(coords_dev, res)
+    nbr = sc.sc_get_neighbor_table(m).cpu().numpy()
+    pairs = sc.sc_map_pairs(m)
+    m.free()
+    return nbr, pairs
+
+
+def test_noalloc_matches_allocating_path_twice(lib):
+    import sparse_voxel_convolution_coord_b300 as sc
+    for key in (3, 2):        # 29,850 voxels, then 20,236 over the same scratch
+        p = synth.make_problem(key)
+        coords = torch.from_numpy(p.coords).cuda()
+        rc, nbr, pairs = noalloc_table(lib, coords, p.res)
+        assert rc == sc.SC_OK, sc.sc_last_error_msg()
+        want, want_pairs = allocating_table(coords, p.res)
+        np.testing.assert_array_equal(nbr, want)
+        assert pairs == want_pairs
+
+
+def test_noalloc_rejects_beyond_limit_and_reports_errors(lib):
+    import sparse_voxel_convolution_coord_b300 as sc
+    coords = torch.zeros((4, 4), dtype=torch.int32, device="cuda")
+    out = torch.empty((4, 27), dtype=torch.int32, device="cuda")
+    rc = lib.sc_build_neighbor_table_noalloc(ctypes.c_void_p(coords.data_ptr()), (1 << 19) + 1,
+                                             16, ctypes.c_void_p(out.data_ptr()), None, None)
+    assert rc == sc.SC_ERR_UNSUPPORTED
+    assert "static scratch limit" in sc.sc_last_error_msg()
+    dup = torch.tensor([[0, 1, 1, 1], [0, 1, 1, 1]], dtype=torch.int32, device="cuda")
+    rc, _, _ = noalloc_table(lib, dup, 4)
+    assert rc == sc.SC_ERR_DUPLICATE
