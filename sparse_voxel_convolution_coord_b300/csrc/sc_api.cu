@@ -52,11 +52,41 @@ bool is_live(sc_map* m) {
   return g_live && g_live->count(m) && m->magic == kMagicLive;
 }
 
+// The library's own stream-ordered pool on `dev`.  Its release threshold is
+// unlimited, so memory freed by sc_free_map stays reserved for the next map
+// instead of being unmapped at the next synchronisation (re-mapping tens of
+// MB costs more than building the map); sc_release_cached_memory trims it.
+constexpr int kMaxPoolDevices = 64;
+std::mutex g_pool_mu;
+cudaMemPool_t g_pools[kMaxPoolDevices] = {};
+
+cudaMemPool_t lib_pool(int dev) {
+  if (dev < 0 || dev >= kMaxPoolDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_pool_mu);
+  if (!g_pools[dev]) {
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    uint64_t keep = ~0ull;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    g_pools[dev] = pool;
+  }
+  return g_pools[dev];
+}
+
 void* dev_alloc(sc_map* m, size_t bytes, cudaStream_t s) {
   if (bytes == 0) bytes = 16;
   if (m->alloc) return m->alloc(bytes, s, m->alloc_ctx);
+  cudaMemPool_t pool = lib_pool(m->device);
   void* p = nullptr;
-  if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
+  if (!pool || cudaMallocFromPoolAsync(&p, bytes, pool, s) != cudaSuccess) {
     cudaGetLastError();
     return nullptr;
   }
@@ -161,7 +191,10 @@ sc_handle sc_build_map(const int32_t* coords, int64_t n, int32_t res, void* stre
     m->hash.bmax = bmax;
     m->hash.n = n;
     m->hash.slots = static_cast<uint64_t*>(dev_alloc(m, cap * sizeof(uint64_t), s));
-    m->nbr = static_cast<int32_t*>(dev_alloc(m, (size_t)n * sc::kTaps * sizeof(int32_t), s));
+    // nbr is padded to whole 128-row tiles (pad rows all -1) so that the
+    // convolution can stage any tile's 13,824-byte block with one bulk copy.
+    m->nbr = static_cast<int32_t*>(
+        dev_alloc(m, (size_t)m->ntiles * sc::kTileRows * sc::kTaps * sizeof(int32_t), s));
     m->tile_mask = static_cast<uint32_t*>(dev_alloc(m, (size_t)m->ntiles * sizeof(uint32_t), s));
     m->d_status = static_cast<uint32_t*>(dev_alloc(m, 16, s));
     if (!m->hash.slots || !m->nbr || !m->tile_mask || !m->d_status) {
@@ -176,7 +209,7 @@ sc_handle sc_build_map(const int32_t* coords, int64_t n, int32_t res, void* stre
     if (e == cudaSuccess) e = sc::launch_hash_insert(coords, m->hash, m->d_status, s);
     if (e == cudaSuccess)
       e = sc::launch_neighbor_query(coords, m->hash, m->nbr, m->tile_mask, m->d_pairs,
-                                    m->d_status, s);
+                                    m->d_status, /*pad_tiles=*/true, s);
     uint32_t host[4] = {0, 0, 0, 0};
     if (e == cudaSuccess) e = cudaMemcpyAsync(host, m->d_status, 16, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);

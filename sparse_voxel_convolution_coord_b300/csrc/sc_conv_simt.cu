@@ -6,75 +6,77 @@
 // accumulation, bias in the same pass).  Used for fp32 inputs, where a
 // tensor-core tf32 product would round the inputs to 10 mantissa bits.
 //
-// One CTA owns 32 output rows and all cout columns; for each offset present
-// in the rows' 128-row tile, 32-wide chunks of the gathered rows and of W[k]
-// are staged in shared memory.  Each output row is written once, no atomics.
+// One warp owns one output row and all cout columns (lane l holds columns
+// l, l+32, ...).  Per 32-channel slice of the input, the warp first issues
+// the 27 gathers of its neighbour rows together (independent loads, one
+// coalesced 128-byte row slice each) into shared memory, then accumulates
+// over the present offsets with W read through L1 (every warp of the grid
+// reads the same W).  Each output row is written once, no atomics.
 #include "sc_internal.cuh"
 
 namespace sc {
 
-constexpr int kSimtRows = 32;
-constexpr int kSimtChunk = 32;
-constexpr int kSimtThreads = 256;
-constexpr int kSimtColsPerThread = 32;  // cout <= 8 * 32 = 256
+constexpr int kSimtWarps = 8;  // output rows per block
 
-__global__ void __launch_bounds__(kSimtThreads) k_conv_simt_f32(
-    const int32_t* __restrict__ nbr, const uint32_t* __restrict__ tile_mask, int64_t n,
-    const float* __restrict__ feats, const float* __restrict__ w, const float* __restrict__ bias,
-    float* __restrict__ out, int cin, int cout) {
-  __shared__ float sA[kSimtRows][kSimtChunk + 1];
-  extern __shared__ float sW[];  // [kSimtChunk][cout]
-  const int64_t row0 = (int64_t)blockIdx.x * kSimtRows;
-  const int r = threadIdx.x >> 3;   // output row within the block
-  const int cg = threadIdx.x & 7;   // column group: columns cg, cg+8, ...
-  float acc[kSimtColsPerThread];
+template <int J>  // columns per lane = J, cout <= 32 * J
+__global__ void __launch_bounds__(kSimtWarps * 32) k_conv_simt_f32(
+    const int32_t* __restrict__ nbr, int64_t n, const float* __restrict__ feats,
+    const float* __restrict__ w, const float* __restrict__ bias, float* __restrict__ out, int cin,
+    int cout) {
+  __shared__ float s_a[kSimtWarps][kTaps][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t o = (int64_t)blockIdx.x * kSimtWarps + warp;
+  if (o >= n) return;  // no block-wide synchronisation below
+  const int32_t nb = lane < kTaps ? __ldg(nbr + o * kTaps + lane) : -1;
+  const uint32_t present = __ballot_sync(0xffffffffu, nb >= 0);
+  float acc[J];
 #pragma unroll
-  for (int j = 0; j < kSimtColsPerThread; ++j) acc[j] = 0.f;
-  const uint32_t mask = tile_mask[row0 / kTileRows];
+  for (int j = 0; j < J; ++j) acc[j] = 0.f;
 
-  for (int k = 0; k < kTaps; ++k) {
-    if (!((mask >> k) & 1u)) continue;
-    for (int c0 = 0; c0 < cin; c0 += kSimtChunk) {
-      for (int e = threadIdx.x; e < kSimtRows * kSimtChunk; e += kSimtThreads) {
-        const int rr = e / kSimtChunk, cc = e % kSimtChunk;
-        const int64_t row = row0 + rr;
-        const int32_t i = row < n ? nbr[row * kTaps + k] : -1;
-        sA[rr][cc] = (i >= 0 && c0 + cc < cin) ? feats[(int64_t)i * cin + c0 + cc] : 0.f;
-      }
-      for (int e = threadIdx.x; e < kSimtChunk * cout; e += kSimtThreads) {
-        const int cc = e / cout, c = e % cout;
-        sW[e] = (c0 + cc < cin) ? w[((int64_t)k * cin + c0 + cc) * cout + c] : 0.f;
-      }
-      __syncthreads();
+  for (int ci0 = 0; ci0 < cin; ci0 += 32) {
+    const int width = min(32, cin - ci0);
+#pragma unroll
+    for (int k = 0; k < kTaps; ++k) {
+      const int32_t i = __shfl_sync(0xffffffffu, nb, k);
+      s_a[warp][k][lane] =
+          (i >= 0 && lane < width) ? __ldg(feats + (int64_t)i * cin + ci0 + lane) : 0.f;
+    }
+    __syncwarp();
+    for (uint32_t rem = present; rem; rem &= rem - 1u) {
+      const int k = __ffs(rem) - 1;
+      const float* wk = w + ((int64_t)k * cin + ci0) * cout + lane;
 #pragma unroll 4
-      for (int cc = 0; cc < kSimtChunk; ++cc) {
-        const float a = sA[r][cc];
+      for (int cc = 0; cc < width; ++cc) {
+        const float a = s_a[warp][k][cc];
+        const float* wr = wk + (int64_t)cc * cout;
 #pragma unroll
-        for (int j = 0; j < kSimtColsPerThread; ++j) {
-          const int c = cg + 8 * j;
-          if (c < cout) acc[j] = fmaf(a, sW[cc * cout + c], acc[j]);
-        }
+        for (int j = 0; j < J; ++j)
+          if (lane + 32 * j < cout) acc[j] = fmaf(a, __ldg(wr + 32 * j), acc[j]);
       }
-      __syncthreads();
     }
+    __syncwarp();
   }
-  const int64_t row = row0 + r;
-  if (row < n) {
 #pragma unroll
-    for (int j = 0; j < kSimtColsPerThread; ++j) {
-      const int c = cg + 8 * j;
-      if (c < cout) out[row * cout + c] = acc[j] + (bias ? bias[c] : 0.f);
-    }
+  for (int j = 0; j < J; ++j) {
+    const int c = lane + 32 * j;
+    if (c < cout) out[o * cout + c] = acc[j] + (bias ? __ldg(bias + c) : 0.f);
   }
 }
 
 cudaError_t launch_conv_simt_f32(const sc_map* m, const float* feats, const float* w,
                                  const float* bias, float* out, int cin, int cout,
                                  cudaStream_t s) {
-  const int64_t blocks = (m->n + kSimtRows - 1) / kSimtRows;
-  const size_t smem = (size_t)kSimtChunk * cout * sizeof(float);
-  k_conv_simt_f32<<<(unsigned)blocks, kSimtThreads, smem, s>>>(m->nbr, m->tile_mask, m->n, feats,
-                                                               w, bias, out, cin, cout);
+  const unsigned blocks = (unsigned)((m->n + kSimtWarps - 1) / kSimtWarps);
+  const int J = (cout + 31) / 32;
+  const dim3 block(kSimtWarps * 32);
+  if (J <= 1)
+    k_conv_simt_f32<1><<<blocks, block, 0, s>>>(m->nbr, m->n, feats, w, bias, out, cin, cout);
+  else if (J <= 2)
+    k_conv_simt_f32<2><<<blocks, block, 0, s>>>(m->nbr, m->n, feats, w, bias, out, cin, cout);
+  else if (J <= 4)
+    k_conv_simt_f32<4><<<blocks, block, 0, s>>>(m->nbr, m->n, feats, w, bias, out, cin, cout);
+  else
+    k_conv_simt_f32<8><<<blocks, block, 0, s>>>(m->nbr, m->n, feats, w, bias, out, cin, cout);
   return cudaGetLastError();
 }
 

@@ -17,12 +17,27 @@
 // into a TMEM accumulator.  Each output row belongs to exactly one tile, so
 // the epilogue (TMEM -> registers, + bias, fp32 store) needs no atomics.
 //
-// CTA = 6 warps, persistent over tiles:
+// Clusters: with CL = 2 the two CTAs of a cluster work on adjacent tiles in
+// lock step (the union of their offset masks) and share each W slice: every
+// CTA loads half of the slice's 64-column boxes and multicasts them to both,
+// halving the L2 -> SM traffic of the weights, which at cin = cout = 256 is
+// two thirds of all operand traffic.  A stage is released only when both
+// CTAs' MMAs have consumed it (each MMA warp commits to the "empty" barrier
+// of both CTAs).
+//
+// CTA = 9 warps, persistent over units of CL tiles:
 //   warps 0-3  epilogue (warp q reads TMEM lanes 32q..32q+31 = rows of the tile)
-//   warp 4     producer: stages the tile's neighbour rows in shared memory,
-//              then per pipeline stage one lane arms the stage barrier and
-//              issues W's boxes, and all 32 lanes issue one gather4 each
-//   warp 5     TMEM allocation; lane 0 issues the MMAs and the commits
+//   warps 4-7  producers: the tile's 128 x 27 neighbour block arrives by one
+//              bulk copy (double-buffered, one unit ahead).  Per pipeline
+//              stage the 128 threads gather the A rows with 16-byte cp.async
+//              copies (8 threads per 128-byte row slice, so each warp
+//              instruction moves four whole lines; absent neighbours are
+//              zero-filled) straight into the swizzled operand layout, and
+//              each thread's mbarrier arrival fires when its copies land.
+//              Thread 0 also issues the W boxes of this CTA by tiled TMA.
+//              (TMA gather4 moves only four 64-128 byte rows per operation;
+//              its per-operation cost, not bandwidth, bounded the gather.)
+//   warp 8     TMEM allocation; lane 0 issues the MMAs and the commits
 // Two TMEM accumulators let the epilogue of one tile overlap the next tile's
 // main loop.  Every wait is bounded (~2 s): a CTA that gives up records
 // SC_ERR_DEVICE_TIMEOUT in the map's status word and leaves cleanly.
@@ -34,26 +49,38 @@
 //     128-byte swizzle; LBO = 8 KB between 64-column blocks, SBO = 1 KB
 //     between 8-row groups.
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
+#include <mutex>
+#include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
 #include "sc_internal.cuh"
 
 namespace sc {
 
-constexpr int kTcThreads = 192;
-constexpr int kSmemBudget = 212 * 1024;
+constexpr int kTcThreads = 288;
+constexpr int kProducerThreads = 128;                   // warps 4-7
+constexpr int kMmaWarp = 8;
+constexpr int kSmemLimit = 227 * 1024;                  // opt-in dynamic shared memory per CTA
+constexpr int kNbrBytes = kTileRows * kTaps * 4;        // one tile's neighbour block, 13,824 B
+constexpr uint64_t kWaitNs = 2000000000ull;             // bounded waits: 2 s
+constexpr uint64_t kDrainNs = 50000000ull;              // final drain after an abort: 50 ms
 
 template <int NPAD, int CS>
 struct TcCfg {
   static constexpr int kSegs = 64 / CS;                 // offset segments per stage
-  static constexpr int kRowBytes = CS * 2;               // one gathered row segment
-  static constexpr int kASeg = kTileRows * kRowBytes;    // bytes per A segment
-  static constexpr int kABytes = kTileRows * 128;        // 16 KB per stage
-  static constexpr int kBBytes = 64 * NPAD * 2;          // 64 K rows x NPAD bf16
+  static constexpr int kRowBytes = CS * 2;              // one gathered row segment
+  static constexpr int kChunks = kRowBytes / 16;        // 16-byte copies per row segment
+  static constexpr int kRowStep = kProducerThreads / kChunks;  // rows per copy pass
+  static constexpr int kASeg = kTileRows * kRowBytes;   // bytes per A segment
+  static constexpr int kABytes = kTileRows * 128;       // 16 KB per stage
+  static constexpr int kBlocksN = NPAD / 64;            // 64-column blocks of B
+  static constexpr int kBBytes = 64 * NPAD * 2;         // 64 K rows x NPAD bf16
+  static constexpr int kBBoxes = kSegs * kBlocksN;      // TMA boxes of B per stage
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kFixed = kTaps * kTileRows * 4 + NPAD * 4 + 1024;  // nbr, bias, bars
-  static constexpr int kStages0 = (kSmemBudget - kFixed - 1024) / kStageBytes;
+  static constexpr int kFixed = 2 * kNbrBytes + NPAD * 4 + 256;  // nbr x2, bias, barriers
+  static constexpr int kStages0 = (kSmemLimit - 1024 - kFixed) / kStageBytes;
   static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kFixed;
   static constexpr uint32_t kTmemCols = (2 * NPAD <= 128) ? 128 : (2 * NPAD <= 256 ? 256 : 512);
@@ -61,12 +88,13 @@ struct TcCfg {
   static constexpr uint32_t kSboA = 8 * kRowBytes;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileRows, NPAD);
   static_assert(kStages >= 2, "pipeline needs two stages");
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
 };
 
 struct TcArgs {
-  const int32_t* nbr;
-  const uint32_t* tile_mask;
+  const __nv_bfloat16* feats;  // [n][cin]
+  const int32_t* nbr;          // [ntiles * 128][27], pad rows -1
+  const uint32_t* tile_mask;   // [ntiles]
   const float* bias;
   float* out;
   uint32_t* status;
@@ -76,10 +104,32 @@ struct TcArgs {
   int cout;
 };
 
-// Stages of a tile: (present offsets) x (cin / 64) when CS == 64, else the
+// Bounded wait with its own limit; ignores the abort flag (used to drain).
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
+// OR of the offset masks of the CL tiles of a unit.
+template <int CL>
+__device__ __forceinline__ uint32_t unit_mask(const uint32_t* tile_mask, int64_t unit,
+                                              int64_t ntiles) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int r = 0; r < CL; ++r) {
+    const int64_t t = unit * CL + r;
+    if (t < ntiles) m |= __ldg(tile_mask + t);
+  }
+  return m;
+}
+
+// Stages of a unit: (present offsets) x (cin / 64) when CS == 64, else the
 // present offsets taken 64/CS at a time.
 template <int CS>
-__device__ __forceinline__ int tile_stages(uint32_t mask, int cin) {
+__device__ __forceinline__ int unit_stages(uint32_t mask, int cin) {
   const int np = __popc(mask);
   if constexpr (CS == 64) {
     return np * (cin >> 6);
@@ -89,109 +139,170 @@ __device__ __forceinline__ int tile_stages(uint32_t mask, int cin) {
   }
 }
 
-// Position of the j-th (0-based) set bit of mask, or 27 when there is none.
-__device__ __forceinline__ int nth_bit(uint32_t mask, int j) {
-  for (int i = 0; i < j && mask; ++i) mask &= mask - 1;
-  return mask ? __ffs(mask) - 1 : kTaps;
-}
-
-template <int NPAD, int CS>
+template <int NPAD, int CS, int CL>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    k_conv_tc(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-              const TcArgs p) {
+    k_conv_tc(const __grid_constant__ CUtensorMap tm_b, const TcArgs p) {
   using C = TcCfg<NPAD, CS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + C::kStages * C::kABytes;
-  int32_t* s_nbr = reinterpret_cast<int32_t*>(sB + C::kStages * C::kBBytes);  // [27][128]
-  float* s_bias = reinterpret_cast<float*>(s_nbr + kTaps * kTileRows);
+  int32_t* s_nbr = reinterpret_cast<int32_t*>(sB + C::kStages * C::kBBytes);  // [2][128][27]
+  float* s_bias = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s_nbr) + 2 * kNbrBytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(s_bias + NPAD);
   uint64_t* empty = full + C::kStages;
   uint64_t* acc_full = empty + C::kStages;
   uint64_t* acc_empty = acc_full + 2;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(acc_empty + 2);
-  __shared__ int s_abort;
+  uint64_t* nbr_full = acc_empty + 2;
+  uint64_t* nbr_empty = nbr_full + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(nbr_empty + 2);
+  int* s_abort = reinterpret_cast<int*>(s_tmem + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
+  const int64_t cid = blockIdx.x / CL;
+  const int64_t ncl = gridDim.x / CL;
+  const int64_t nunits = (p.ntiles + CL - 1) / CL;
+  constexpr uint16_t kAllCtas = (uint16_t)((1u << CL) - 1u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&full[s], kProducerThreads + 1);  // 128 cp.async arrivals + the W expect_tx
+      mbar_init(&empty[s], CL);  // one commit from the MMA warp of every CTA of the cluster
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], kTileRows);
+      mbar_init(&nbr_full[a], 1);
+      mbar_init(&nbr_empty[a], kProducerThreads);
     }
-    s_abort = 0;
+    *s_abort = 0;
     fence_barrier_init();
   }
-  if (warp == 5) tmem_alloc(s_tmem, C::kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(s_tmem, C::kTmemCols);
   for (int i = threadIdx.x; i < NPAD; i += kTcThreads)
     s_bias[i] = (p.bias != nullptr && i < p.cout) ? p.bias[i] : 0.f;
-  if (warp == 4 && lane == 0) {
-    prefetch_tensormap(&tm_a);
-    prefetch_tensormap(&tm_b);
-  }
+  if (warp == 4 && lane == 0) prefetch_tensormap(&tm_b);
   tc_fence_before();
   __syncthreads();
+  if constexpr (CL > 1) cluster_sync_all();  // peers' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
-  volatile int* abort_flag = &s_abort;
+  volatile int* abort_flag = s_abort;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    const int32_t oob = (int32_t)p.n;  // a row index past the end: TMA fills zeros
-    uint32_t stage = 0, phase = 0;
+  if (warp >= 4 && warp < kMmaWarp) {
+    // ------------------------------------------------------------ producers
+    const int pt = threadIdx.x - 128;           // 0..127
+    const int chunk_id = pt % C::kChunks;       // which 16 bytes of a row segment
+    const int row_first = pt / C::kChunks;      // rows row_first + kRowStep * i
+    const int cblocks = p.cin >> 6;             // 64-channel blocks per offset (CS == 64)
+    const __nv_bfloat16* feats = p.feats;
+    uint32_t stage = 0, phase = 0, nbr_phase = 0;
+    int buf = 0;
     bool ok = true;
-    for (int64_t tile = blockIdx.x; tile < p.ntiles && ok; tile += gridDim.x) {
-      const int64_t row0 = tile * kTileRows;
-      const uint32_t mask = p.tile_mask[tile];
-      const int nst = tile_stages<CS>(mask, p.cin);
-      __syncwarp();
-      for (int e = lane; e < kTileRows * kTaps; e += 32) {
-        const int r = e / kTaps, k = e - r * kTaps;
-        const int64_t row = row0 + r;
-        const int32_t v = row < p.n ? __ldg(p.nbr + row0 * kTaps + e) : -1;
-        s_nbr[k * kTileRows + r] = v < 0 ? oob : v;
+    uint32_t fills = 0;  // thread 0: bit b = parity of the fills of neighbour buffer b
+    // Thread 0 refills buffer b with the neighbour block of `unit`'s tile once
+    // every producer thread has released the buffer's previous contents.
+    auto issue_nbr = [&](int64_t unit, int b, uint32_t& nfills) -> bool {
+      const int64_t t = unit * CL + rank;
+      if (pt != 0 || unit >= nunits || t >= p.ntiles) return true;
+      if ((nfills >> (2 + b)) & 1u) {  // buffer used before: wait for its release
+        if (!mbar_wait_bounded(&nbr_empty[b], ((nfills >> b) & 1u) ^ 1u, abort_flag))
+          return false;
       }
-      __syncwarp();
+      mbar_arrive_expect_tx(&nbr_full[b], kNbrBytes);
+      bulk_copy_g2s(s_nbr + b * kTileRows * kTaps, p.nbr + t * (kTileRows * kTaps), kNbrBytes,
+                    &nbr_full[b]);
+      nfills ^= 1u << b;         // parity of fills
+      nfills |= 1u << (2 + b);   // used at least once
+      return true;
+    };
+    ok = issue_nbr(cid, 0, fills);
+    for (int64_t unit = cid; unit < nunits && ok; unit += ncl) {
+      const int64_t tile = unit * CL + rank;
+      const bool has_rows = tile < p.ntiles;
+      const uint32_t mask = unit_mask<CL>(p.tile_mask, unit, p.ntiles);
+      const int nst = unit_stages<CS>(mask, p.cin);
+      if (!issue_nbr(unit + ncl, buf ^ 1, fills)) {
+        ok = false;
+        break;
+      }
+      if (has_rows) {
+        if (!mbar_wait_bounded(&nbr_full[buf], (nbr_phase >> buf) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        nbr_phase ^= 1u << buf;
+      }
+      const int32_t* nb = s_nbr + buf * (kTileRows * kTaps);
+      uint32_t rem = mask;
+      int cblk = 0;
       for (int s = 0; s < nst; ++s) {
         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-        __syncwarp();
         uint8_t* a_st = sA + stage * C::kABytes;
         uint8_t* b_st = sB + stage * C::kBBytes;
+        int ks[C::kSegs];
+        int c0 = 0;
 #pragma unroll
         for (int j = 0; j < C::kSegs; ++j) {
-          int k, c0;
           if constexpr (CS == 64) {
-            const int chunks = p.cin >> 6;
-            k = nth_bit(mask, s / chunks);
-            c0 = (s % chunks) * 64;
+            ks[j] = __ffs(rem) - 1;
+            c0 = cblk * 64;
           } else {
-            k = nth_bit(mask, s * C::kSegs + j);
-            c0 = 0;
+            ks[j] = rem ? __ffs(rem) - 1 : kTaps;  // kTaps: padding segment, all zeros
+            rem &= rem - 1u;
           }
-          int4 rows;
-          if (k < kTaps)
-            rows = *reinterpret_cast<const int4*>(&s_nbr[k * kTileRows + 4 * lane]);
-          else
-            rows = make_int4(oob, oob, oob, oob);
-          tma_gather4(a_st + j * C::kASeg + lane * 4 * C::kRowBytes, &tm_a, &full[stage], c0,
-                      rows);
-          if (lane == 0) {
-            // k == 27 addresses rows past W's end: the box is zero-filled.
+        }
+        // A: 16-byte copies into the swizzled K-major layout.  Row r of a
+        // segment starts at r * kRowBytes; its 16-byte chunk c lands at chunk
+        // c ^ ((r * kRowBytes >> 7) & (kChunks - 1)) (the 128/64/32-byte
+        // swizzle of the operand descriptors).
 #pragma unroll
-            for (int nb = 0; nb < NPAD / 64; ++nb)
-              tma_load_2d(b_st + nb * (64 * 128) + j * CS * 128, &tm_b, &full[stage], nb * 64,
-                          k * p.cin + c0);
+        for (int j = 0; j < C::kSegs; ++j) {
+          const int k = ks[j];
+          uint8_t* seg = a_st + j * C::kASeg;
+#pragma unroll
+          for (int i = 0; i < C::kChunks; ++i) {
+            const int r = row_first + C::kRowStep * i;
+            const int32_t src_row = (has_rows && k < kTaps) ? nb[r * kTaps + k] : -1;
+            const int sw = (r * C::kRowBytes >> 7) & (C::kChunks - 1);
+            uint8_t* dst = seg + r * C::kRowBytes + ((chunk_id ^ sw) << 4);
+            const __nv_bfloat16* src =
+                src_row >= 0 ? feats + (int64_t)src_row * p.cin + c0 + chunk_id * 8 : feats;
+            cp_async_16(dst, src, src_row >= 0 ? 16u : 0u);
+          }
+        }
+        cp_async_arrive_noinc(&full[stage]);
+        if (pt == 0) {
+          // W: this CTA's share of the stage's 64-column boxes (multicast to
+          // the cluster when CL > 1); the expect_tx covers every box.
+          mbar_arrive_expect_tx(&full[stage], C::kBBytes);
+#pragma unroll
+          for (int j = 0; j < C::kSegs; ++j) {
+#pragma unroll
+            for (int nb2 = 0; nb2 < C::kBlocksN; ++nb2) {
+              const int b = j * C::kBlocksN + nb2;
+              if ((uint32_t)(b % CL) == rank) {
+                // k == 27 addresses rows past W's end: the box is zero-filled.
+                uint8_t* dst = b_st + nb2 * (64 * 128) + j * CS * 128;
+                const int32_t y = ks[j] * p.cin + c0;
+                if constexpr (CL > 1)
+                  tma_load_2d_multicast(dst, &tm_b, &full[stage], nb2 * 64, y, kAllCtas);
+                else
+                  tma_load_2d(dst, &tm_b, &full[stage], nb2 * 64, y);
+              }
+            }
+          }
+        }
+        if constexpr (CS == 64) {
+          if (++cblk == cblocks) {
+            cblk = 0;
+            rem &= rem - 1u;
           }
         }
         if (++stage == C::kStages) {
@@ -199,19 +310,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           phase ^= 1u;
         }
       }
+      if (!ok) break;
+      if (has_rows) mbar_arrive(&nbr_empty[buf]);  // this thread is done with the block
+      buf ^= 1;
     }
-    if (!ok && lane == 0) {
-      s_abort = 1;
-      atomicOr(p.status, kStatTimeout);
+    if (!ok) {
+      *s_abort = 1;
+      if (pt == 0) atomicOr(p.status, kStatTimeout);
     }
-  } else if (warp == 5) {
+    // Drain: wait until every stage this CTA armed has been released by the
+    // MMA warps of all CTAs of the cluster, so that no copy or commit aimed at
+    // this CTA's shared memory is still in flight when it exits.
+    cp_async_wait<0>();
+    if (warp == 4) {
+      for (int i = 0; i < C::kStages; ++i) {
+        if (!mbar_wait_for(&empty[stage], phase ^ 1u, ok ? kWaitNs : kDrainNs)) {
+          if (lane == 0) atomicOr(p.status, kStatTimeout);
+          break;
+        }
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int64_t tile = blockIdx.x; tile < p.ntiles && ok; tile += gridDim.x) {
-        const int nst = tile_stages<CS>(p.tile_mask[tile], p.cin);
+      for (int64_t unit = cid; unit < nunits && ok; unit += ncl) {
+        const int nst = unit_stages<CS>(unit_mask<CL>(p.tile_mask, unit, p.ntiles), p.cin);
         if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -224,6 +354,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           tc_fence_after();
+          fence_proxy_async_smem();  // the A rows were written by cp.async (generic proxy)
           const uint32_t a_base = smem_u32(sA + stage * C::kABytes);
           const uint32_t b_base = smem_u32(sB + stage * C::kBBytes);
 #pragma unroll
@@ -236,7 +367,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               tc_mma_bf16(d_tmem, ad, bd, C::kIdesc, (s | j | kk) != 0 ? 1u : 0u);
             }
           }
-          tc_commit(&empty[stage]);
+          if constexpr (CL > 1)
+            tc_commit_multicast(&empty[stage], kAllCtas);
+          else
+            tc_commit(&empty[stage]);
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
@@ -248,7 +382,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (acc == 0) acc_phase ^= 1u;
       }
       if (!ok) {
-        s_abort = 1;
+        *s_abort = 1;
         atomicOr(p.status, kStatTimeout);
       }
     }
@@ -258,13 +392,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t acc = 0, acc_phase = 0;
     bool ok = true;
     const int nchunks = (p.cout + 31) >> 5;
-    for (int64_t tile = blockIdx.x; tile < p.ntiles && ok; tile += gridDim.x) {
+    for (int64_t unit = cid; unit < nunits && ok; unit += ncl) {
       if (!mbar_wait_bounded(&acc_full[acc], acc_phase, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int64_t row = tile * kTileRows + warp * 32 + lane;
+      const int64_t row = (unit * CL + rank) * kTileRows + warp * 32 + lane;
       const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + acc * NPAD;
       float* orow = p.out + row * p.cout;
       for (int ch = 0; ch < nchunks; ++ch) {
@@ -292,14 +426,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (acc == 0) acc_phase ^= 1u;
     }
     if (!ok && lane == 0) {
-      s_abort = 1;
+      *s_abort = 1;
       atomicOr(p.status, kStatTimeout);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if constexpr (CL > 1) cluster_sync_all();  // no peer traffic is aimed at this CTA any more
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
   }
@@ -338,39 +473,77 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
   return r == CUDA_SUCCESS;
 }
 
-int num_sms() {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 148;
-  }
-  return sms;
+constexpr int kMaxDev = 64;
+
+// Per device and kernel instantiation: the shared-memory attribute is set
+// once and the number of co-resident clusters is queried once.
+struct LaunchCache {
+  std::mutex mu;
+  int max_clusters[kMaxDev] = {};
+};
+
+// Cluster size for the weight multicast.  Default: pairs when a W slice has
+// at least two 64-column boxes to split (cout > 64), single CTAs otherwise.
+// SC_CONV_CLUSTER=1|2 overrides it.
+int cluster_size(int npad) {
+  static int forced = [] {
+    const char* e = std::getenv("SC_CONV_CLUSTER");
+    const int v = e ? std::atoi(e) : 0;
+    return (v == 1 || v == 2) ? v : 0;
+  }();
+  if (forced) return forced;
+  return npad > 64 ? 2 : 1;
 }
 
-template <int NPAD, int CS>
+template <int NPAD, int CS, int CL>
 cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, const float* bias,
                          float* out, int cin, int cout, cudaStream_t s) {
   using C = TcCfg<NPAD, CS>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_conv_tc<NPAD, CS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
+  auto kern = k_conv_tc<NPAD, CS, CL>;
+  static LaunchCache cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+
+  int max_clusters;
+  {
+    std::lock_guard<std::mutex> lk(cache.mu);
+    if (cache.max_clusters[dev] == 0) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+      if (e != cudaSuccess) return e;
+      int sms = 148;
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      cfg.gridDim = dim3(CL * (sms / CL), 1, 1);
+      int nc = 0;
+      if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess || nc <= 0) {
+        cudaGetLastError();
+        nc = sms / CL;
+      }
+      cache.max_clusters[dev] = nc;
+    }
+    max_clusters = cache.max_clusters[dev];
   }
-  alignas(64) CUtensorMap tm_a, tm_b;
-  const CUtensorMapSwizzle swz_a = CS == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
-                                   : CS == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                              : CU_TENSOR_MAP_SWIZZLE_32B;
-  if (!encode_2d(&tm_a, feats, (uint64_t)cin, (uint64_t)m->n, (uint64_t)cin * 2, CS, 1, swz_a))
-    return cudaErrorInvalidValue;
+
+  alignas(64) CUtensorMap tm_b;
   if (!encode_2d(&tm_b, w, (uint64_t)cout, (uint64_t)kTaps * cin, (uint64_t)cout * 2, 64, CS,
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   TcArgs a;
+  a.feats = static_cast<const __nv_bfloat16*>(feats);
   a.nbr = m->nbr;
   a.tile_mask = m->tile_mask;
   a.bias = bias;
@@ -380,17 +553,27 @@ cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, cons
   a.ntiles = m->ntiles;
   a.cin = cin;
   a.cout = cout;
-  const int grid = (int)std::min<int64_t>(m->ntiles, num_sms());
-  k_conv_tc<NPAD, CS><<<grid, kTcThreads, C::kSmemBytes, s>>>(tm_a, tm_b, a);
-  return cudaGetLastError();
+  const int64_t nunits = (m->ntiles + CL - 1) / CL;
+  cfg.gridDim = dim3((unsigned)(CL * std::min<int64_t>(nunits, max_clusters)), 1, 1);
+  void* args[2] = {&tm_b, &a};
+  e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kern), args);
+  return e;
+}
+
+template <int NPAD, int CS>
+cudaError_t launch_cl(const sc_map* m, const void* feats, const void* w, const float* bias,
+                      float* out, int cin, int cout, cudaStream_t s) {
+  if (cluster_size(NPAD) == 2)
+    return launch_typed<NPAD, CS, 2>(m, feats, w, bias, out, cin, cout, s);
+  return launch_typed<NPAD, CS, 1>(m, feats, w, bias, out, cin, cout, s);
 }
 
 template <int NPAD>
 cudaError_t launch_npad(const sc_map* m, const void* feats, const void* w, const float* bias,
                         float* out, int cin, int cout, cudaStream_t s) {
-  if (cin == 16) return launch_typed<NPAD, 16>(m, feats, w, bias, out, cin, cout, s);
-  if (cin == 32) return launch_typed<NPAD, 32>(m, feats, w, bias, out, cin, cout, s);
-  return launch_typed<NPAD, 64>(m, feats, w, bias, out, cin, cout, s);
+  if (cin == 16) return launch_cl<NPAD, 16>(m, feats, w, bias, out, cin, cout, s);
+  if (cin == 32) return launch_cl<NPAD, 32>(m, feats, w, bias, out, cin, cout, s);
+  return launch_cl<NPAD, 64>(m, feats, w, bias, out, cin, cout, s);
 }
 
 }  // namespace

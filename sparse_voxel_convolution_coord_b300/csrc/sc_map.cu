@@ -112,7 +112,8 @@ __device__ __forceinline__ int32_t finish_probe(const HashParams& hp, uint64_t k
 
 __global__ void __launch_bounds__(kTileRows) k_neighbor_query(
     const int4* __restrict__ coords, HashParams hp, int32_t* __restrict__ nbr,
-    uint32_t* __restrict__ tile_mask, unsigned long long* pair_count, uint32_t* status) {
+    uint32_t* __restrict__ tile_mask, unsigned long long* pair_count, uint32_t* status,
+    bool pad_tiles) {
   __shared__ __align__(16) int32_t s_nbr[kTileRows * kTaps];
   __shared__ uint32_t s_or[kTileRows / 32];
   __shared__ uint32_t s_cnt[kTileRows / 32];
@@ -150,6 +151,9 @@ __global__ void __launch_bounds__(kTileRows) k_neighbor_query(
       s_nbr[threadIdx.x * kTaps + k] = r;
       mask |= (r >= 0 ? 1u : 0u) << k;
     }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kTaps; ++k) s_nbr[threadIdx.x * kTaps + k] = -1;
   }
   const uint32_t wor = __reduce_or_sync(0xffffffffu, mask);
   const uint32_t wcnt = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(mask));
@@ -167,7 +171,7 @@ __global__ void __launch_bounds__(kTileRows) k_neighbor_query(
     tile_mask[blockIdx.x] = m;
     atomicAdd(pair_count, (unsigned long long)cnt);
   }
-  const int64_t rows = min((int64_t)kTileRows, hp.n - row0);
+  const int64_t rows = pad_tiles ? (int64_t)kTileRows : min((int64_t)kTileRows, hp.n - row0);
   const int total = (int)rows * kTaps;
   int32_t* dst = nbr + row0 * kTaps;  // 16-byte aligned: row0 * 27 * 4 = blockIdx * 13824
   const int nvec = total >> 2;
@@ -189,11 +193,11 @@ cudaError_t launch_hash_insert(const int32_t* coords, const HashParams& hp, uint
 
 cudaError_t launch_neighbor_query(const int32_t* coords, const HashParams& hp, int32_t* nbr,
                                   uint32_t* tile_mask, unsigned long long* pair_count,
-                                  uint32_t* status, cudaStream_t s) {
+                                  uint32_t* status, bool pad_tiles, cudaStream_t s) {
   if (hp.n == 0) return cudaSuccess;
   const int64_t blocks = (hp.n + kTileRows - 1) / kTileRows;
   k_neighbor_query<<<(unsigned)blocks, kTileRows, 0, s>>>(
-      reinterpret_cast<const int4*>(coords), hp, nbr, tile_mask, pair_count, status);
+      reinterpret_cast<const int4*>(coords), hp, nbr, tile_mask, pair_count, status, pad_tiles);
   return cudaGetLastError();
 }
 

@@ -114,7 +114,8 @@ extern "C" SC_API sc_status sc_build_neighbor_table_noalloc(const int32_t* coord
   if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, 16, s);
   if (e == cudaSuccess) e = sc::launch_hash_insert(coords, hp, status, s);
   if (e == cudaSuccess)
-    e = sc::launch_neighbor_query(coords, hp, nbr_out, tile_mask, pair_count, status, s);
+    e = sc::launch_neighbor_query(coords, hp, nbr_out, tile_mask, pair_count, status,
+                                  /*pad_tiles=*/false, s);
   uint32_t host[4] = {0, 0, 0, 0};
   if (e == cudaSuccess) e = cudaMemcpyAsync(host, status, 16, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
