@@ -25,19 +25,20 @@
 // CTAs' MMAs have consumed it (each MMA warp commits to the "empty" barrier
 // of both CTAs).
 //
-// CTA = 9 warps, persistent over units of CL tiles:
+// CTA = 14 warps, persistent over units of CL tiles:
 //   warps 0-3  epilogue (warp q reads TMEM lanes 32q..32q+31 = rows of the tile)
-//   warps 4-7  producers: the tile's 128 x 27 neighbour block arrives by one
-//              bulk copy (double-buffered, one unit ahead).  Per pipeline
-//              stage the 128 threads gather the A rows with 16-byte cp.async
-//              copies (8 threads per 128-byte row slice, so each warp
-//              instruction moves four whole lines; absent neighbours are
-//              zero-filled) straight into the swizzled operand layout, and
-//              each thread's mbarrier arrival fires when its copies land.
-//              Thread 0 also issues the W boxes of this CTA by tiled TMA.
-//              (TMA gather4 moves only four 64-128 byte rows per operation;
-//              its per-operation cost, not bandwidth, bounded the gather.)
-//   warp 8     TMEM allocation; lane 0 issues the MMAs and the commits
+//   warp 4     loader: the tile's 128 x 27 neighbour block by one bulk copy
+//              (double-buffered, one unit ahead) and, per stage, this CTA's
+//              W boxes by tiled TMA
+//   warps 5-12 A producers: per pipeline stage the 256 threads gather the
+//              A rows with 16-byte cp.async copies (consecutive threads take
+//              consecutive 16-byte chunks of a row, so a warp instruction
+//              moves whole lines; absent neighbours are zero-filled) straight
+//              into the swizzled operand layout; each thread's mbarrier
+//              arrival fires when its copies land.  (TMA gather4 moves only
+//              four 64-128 byte rows per operation; its per-operation cost,
+//              not bandwidth, bounded the gather.)
+//   warp 13    TMEM allocation; lane 0 issues the MMAs and the commits
 // Two TMEM accumulators let the epilogue of one tile overlap the next tile's
 // main loop.  Every wait is bounded (~2 s): a CTA that gives up records
 // SC_ERR_DEVICE_TIMEOUT in the map's status word and leaves cleanly.
@@ -59,9 +60,15 @@
 
 namespace sc {
 
-constexpr int kTcThreads = 288;
-constexpr int kProducerThreads = 128;                   // warps 4-7
-constexpr int kMmaWarp = 8;
+#ifndef SC_PRODUCER_WARPS
+#define SC_PRODUCER_WARPS 8
+#endif
+constexpr int kLoaderWarp = 4;                          // W boxes + neighbour blocks
+constexpr int kProducerWarps = SC_PRODUCER_WARPS;       // A gathers: warps 5 .. 4 + kProducerWarps
+constexpr int kProducerThreads = 32 * kProducerWarps;
+constexpr int kMmaWarp = 5 + kProducerWarps;
+constexpr int kTcThreads = 32 * (kMmaWarp + 1);
+
 constexpr int kSmemLimit = 227 * 1024;                  // opt-in dynamic shared memory per CTA
 constexpr int kNbrBytes = kTileRows * kTaps * 4;        // one tile's neighbour block, 13,824 B
 constexpr uint64_t kWaitNs = 2000000000ull;             // bounded waits: 2 s
@@ -72,7 +79,11 @@ struct TcCfg {
   static constexpr int kSegs = 64 / CS;                 // offset segments per stage
   static constexpr int kRowBytes = CS * 2;              // one gathered row segment
   static constexpr int kChunks = kRowBytes / 16;        // 16-byte copies per row segment
-  static constexpr int kRowStep = kProducerThreads / kChunks;  // rows per copy pass
+  static constexpr int kSegCopies = kTileRows * kChunks;        // 16-byte copies per segment
+  static constexpr int kPerThread = kSegs * kSegCopies / kProducerThreads;
+  static_assert(kPerThread * kProducerThreads == kSegs * kSegCopies &&
+                    kProducerThreads % kChunks == 0,
+                "producer threads must tile the stage's copies");
   static constexpr int kASeg = kTileRows * kRowBytes;   // bytes per A segment
   static constexpr int kABytes = kTileRows * 128;       // 16 KB per stage
   static constexpr int kBlocksN = NPAD / 64;            // 64-column blocks of B
@@ -139,6 +150,35 @@ __device__ __forceinline__ int unit_stages(uint32_t mask, int cin) {
   }
 }
 
+// Walks the K slices of a unit in order: for CS == 64, each present offset
+// k (ascending) with its cin/64 channel blocks; for CS < 64, the present
+// offsets 64/CS at a time (kTaps pads the last stage).  next() fills the
+// stage's offsets and returns its first channel.
+template <int CS>
+struct OffsetIter {
+  uint32_t rem;
+  int cblk = 0, cblocks;
+  __device__ __forceinline__ OffsetIter(uint32_t mask, int cin) : rem(mask), cblocks(cin >> 6) {}
+  __device__ __forceinline__ int next(int (&ks)[64 / CS]) {
+    if constexpr (CS == 64) {
+      ks[0] = __ffs(rem) - 1;
+      const int c0 = cblk * 64;
+      if (++cblk == cblocks) {
+        cblk = 0;
+        rem &= rem - 1u;
+      }
+      return c0;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 64 / CS; ++j) {
+        ks[j] = rem ? __ffs(rem) - 1 : kTaps;
+        rem &= rem - 1u;
+      }
+      return 0;
+    }
+  }
+};
+
 template <int NPAD, int CS, int CL>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_conv_tc(const __grid_constant__ CUtensorMap tm_b, const TcArgs p) {
@@ -169,7 +209,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&full[s], kProducerThreads + 1);  // 128 cp.async arrivals + the W expect_tx
+      mbar_init(&full[s], kProducerThreads + 1);  // one per A producer + the loader's expect_tx
       mbar_init(&empty[s], CL);  // one commit from the MMA warp of every CTA of the cluster
     }
     for (int a = 0; a < 2; ++a) {
@@ -184,7 +224,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == kMmaWarp) tmem_alloc(s_tmem, C::kTmemCols);
   for (int i = threadIdx.x; i < NPAD; i += kTcThreads)
     s_bias[i] = (p.bias != nullptr && i < p.cout) ? p.bias[i] : 0.f;
-  if (warp == 4 && lane == 0) prefetch_tensormap(&tm_b);
+  if (warp == kLoaderWarp && lane == 0) prefetch_tensormap(&tm_b);
   tc_fence_before();
   __syncthreads();
   if constexpr (CL > 1) cluster_sync_all();  // peers' barriers exist before any multicast
@@ -192,96 +232,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem_base = *s_tmem;
   volatile int* abort_flag = s_abort;
 
-  if (warp >= 4 && warp < kMmaWarp) {
-    // ------------------------------------------------------------ producers
-    const int pt = threadIdx.x - 128;           // 0..127
-    const int chunk_id = pt % C::kChunks;       // which 16 bytes of a row segment
-    const int row_first = pt / C::kChunks;      // rows row_first + kRowStep * i
-    const int cblocks = p.cin >> 6;             // 64-channel blocks per offset (CS == 64)
-    const __nv_bfloat16* feats = p.feats;
-    uint32_t stage = 0, phase = 0, nbr_phase = 0;
-    int buf = 0;
-    bool ok = true;
-    uint32_t fills = 0;  // thread 0: bit b = parity of the fills of neighbour buffer b
-    // Thread 0 refills buffer b with the neighbour block of `unit`'s tile once
-    // every producer thread has released the buffer's previous contents.
-    auto issue_nbr = [&](int64_t unit, int b, uint32_t& nfills) -> bool {
-      const int64_t t = unit * CL + rank;
-      if (pt != 0 || unit >= nunits || t >= p.ntiles) return true;
-      if ((nfills >> (2 + b)) & 1u) {  // buffer used before: wait for its release
-        if (!mbar_wait_bounded(&nbr_empty[b], ((nfills >> b) & 1u) ^ 1u, abort_flag))
-          return false;
-      }
-      mbar_arrive_expect_tx(&nbr_full[b], kNbrBytes);
-      bulk_copy_g2s(s_nbr + b * kTileRows * kTaps, p.nbr + t * (kTileRows * kTaps), kNbrBytes,
-                    &nbr_full[b]);
-      nfills ^= 1u << b;         // parity of fills
-      nfills |= 1u << (2 + b);   // used at least once
-      return true;
-    };
-    ok = issue_nbr(cid, 0, fills);
-    for (int64_t unit = cid; unit < nunits && ok; unit += ncl) {
-      const int64_t tile = unit * CL + rank;
-      const bool has_rows = tile < p.ntiles;
-      const uint32_t mask = unit_mask<CL>(p.tile_mask, unit, p.ntiles);
-      const int nst = unit_stages<CS>(mask, p.cin);
-      if (!issue_nbr(unit + ncl, buf ^ 1, fills)) {
-        ok = false;
-        break;
-      }
-      if (has_rows) {
-        if (!mbar_wait_bounded(&nbr_full[buf], (nbr_phase >> buf) & 1u, abort_flag)) {
+  if (warp == kLoaderWarp) {
+    // ------------------------------------------------------------ loader
+    // Lane 0: the neighbour block of each unit's tile (bulk copy, one unit
+    // ahead) and, per stage, this CTA's W boxes by tiled TMA.
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, fills = 0;
+      int buf = 0;
+      bool ok = true;
+      // Refill buffer b once every A producer has released its contents.
+      auto issue_nbr = [&](int64_t unit, int b) -> bool {
+        const int64_t t = unit * CL + rank;
+        if (unit >= nunits || t >= p.ntiles) return true;
+        if ((fills >> (2 + b)) & 1u) {  // used before: wait for the release
+          if (!mbar_wait_bounded(&nbr_empty[b], ((fills >> b) & 1u) ^ 1u, abort_flag))
+            return false;
+        }
+        mbar_arrive_expect_tx(&nbr_full[b], kNbrBytes);
+        bulk_copy_g2s(s_nbr + b * kTileRows * kTaps, p.nbr + t * (kTileRows * kTaps), kNbrBytes,
+                      &nbr_full[b]);
+        fills ^= 1u << b;        // parity of the fills of buffer b
+        fills |= 1u << (2 + b);  // buffer b used at least once
+        return true;
+      };
+      ok = issue_nbr(cid, 0);
+      for (int64_t unit = cid; unit < nunits && ok; unit += ncl) {
+        const uint32_t mask = unit_mask<CL>(p.tile_mask, unit, p.ntiles);
+        const int nst = unit_stages<CS>(mask, p.cin);
+        if (!issue_nbr(unit + ncl, buf ^ 1)) {
           ok = false;
           break;
         }
-        nbr_phase ^= 1u << buf;
-      }
-      const int32_t* nb = s_nbr + buf * (kTileRows * kTaps);
-      uint32_t rem = mask;
-      int cblk = 0;
-      for (int s = 0; s < nst; ++s) {
-        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        uint8_t* a_st = sA + stage * C::kABytes;
-        uint8_t* b_st = sB + stage * C::kBBytes;
-        int ks[C::kSegs];
-        int c0 = 0;
-#pragma unroll
-        for (int j = 0; j < C::kSegs; ++j) {
-          if constexpr (CS == 64) {
-            ks[j] = __ffs(rem) - 1;
-            c0 = cblk * 64;
-          } else {
-            ks[j] = rem ? __ffs(rem) - 1 : kTaps;  // kTaps: padding segment, all zeros
-            rem &= rem - 1u;
+        OffsetIter<CS> it(mask, p.cin);
+        for (int s = 0; s < nst; ++s) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
           }
-        }
-        // A: 16-byte copies into the swizzled K-major layout.  Row r of a
-        // segment starts at r * kRowBytes; its 16-byte chunk c lands at chunk
-        // c ^ ((r * kRowBytes >> 7) & (kChunks - 1)) (the 128/64/32-byte
-        // swizzle of the operand descriptors).
-#pragma unroll
-        for (int j = 0; j < C::kSegs; ++j) {
-          const int k = ks[j];
-          uint8_t* seg = a_st + j * C::kASeg;
-#pragma unroll
-          for (int i = 0; i < C::kChunks; ++i) {
-            const int r = row_first + C::kRowStep * i;
-            const int32_t src_row = (has_rows && k < kTaps) ? nb[r * kTaps + k] : -1;
-            const int sw = (r * C::kRowBytes >> 7) & (C::kChunks - 1);
-            uint8_t* dst = seg + r * C::kRowBytes + ((chunk_id ^ sw) << 4);
-            const __nv_bfloat16* src =
-                src_row >= 0 ? feats + (int64_t)src_row * p.cin + c0 + chunk_id * 8 : feats;
-            cp_async_16(dst, src, src_row >= 0 ? 16u : 0u);
-          }
-        }
-        cp_async_arrive_noinc(&full[stage]);
-        if (pt == 0) {
-          // W: this CTA's share of the stage's 64-column boxes (multicast to
-          // the cluster when CL > 1); the expect_tx covers every box.
+          // The expect_tx covers every box of the stage, including those the
+          // peer CTA multicasts here.
           mbar_arrive_expect_tx(&full[stage], C::kBBytes);
+          uint8_t* b_st = sB + stage * C::kBBytes;
+          int ks[C::kSegs];
+          const int c0 = it.next(ks);
 #pragma unroll
           for (int j = 0; j < C::kSegs; ++j) {
 #pragma unroll
@@ -298,13 +291,94 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               }
             }
           }
-        }
-        if constexpr (CS == 64) {
-          if (++cblk == cblocks) {
-            cblk = 0;
-            rem &= rem - 1u;
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
+        buf ^= 1;
+      }
+      if (!ok) {
+        *s_abort = 1;
+        atomicOr(p.status, kStatTimeout);
+      }
+      // Drain: wait until every stage armed here has been released by the MMA
+      // warps of all CTAs of the cluster, so that no copy or commit aimed at
+      // this CTA's shared memory is still in flight when it exits.
+      for (int i = 0; i < C::kStages; ++i) {
+        if (!mbar_wait_for(&empty[stage], phase ^ 1u, ok ? kWaitNs : kDrainNs)) {
+          atomicOr(p.status, kStatTimeout);
+          break;
+        }
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp > kLoaderWarp && warp < kMmaWarp) {
+    // ------------------------------------------------------------ A producers
+    const int pt = threadIdx.x - 32 * (kLoaderWarp + 1);  // 0 .. kProducerThreads - 1
+    const int chunk_id = pt % C::kChunks;       // which 16 bytes of a row segment
+    const __nv_bfloat16* feats = p.feats;
+    uint32_t stage = 0, phase = 0, nbr_phase = 0;
+    int buf = 0;
+    bool ok = true;
+    for (int64_t unit = cid; unit < nunits && ok; unit += ncl) {
+      const int64_t tile = unit * CL + rank;
+      const bool has_rows = tile < p.ntiles;
+      const uint32_t mask = unit_mask<CL>(p.tile_mask, unit, p.ntiles);
+      const int nst = unit_stages<CS>(mask, p.cin);
+      if (has_rows) {
+        if (!mbar_wait_bounded(&nbr_full[buf], (nbr_phase >> buf) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        nbr_phase ^= 1u << buf;
+      }
+      const int32_t* nb = s_nbr + buf * (kTileRows * kTaps);
+      OffsetIter<CS> it(mask, p.cin);
+      for (int s = 0; s < nst; ++s) {
+        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint8_t* a_st = sA + stage * C::kABytes;
+        int ks[C::kSegs];
+        const int c0 = it.next(ks);
+        // The stage's kSegs x 128 rows x kChunks 16-byte copies, thread pt
+        // taking copies pt, pt + kProducerThreads, ... (consecutive threads:
+        // consecutive chunks of one row).  Row r of a segment starts at
+        // r * kRowBytes; its chunk c lands at c ^ ((r * kRowBytes >> 7) &
+        // (kChunks - 1)) (the 128/64/32-byte swizzle of the operand
+        // descriptors).  Absent neighbours copy a row of zeros.
+        int32_t src_rows[C::kPerThread];
+#pragma unroll
+        for (int i = 0; i < C::kPerThread; ++i) {
+          const int q = pt + i * kProducerThreads;
+          const int j = q / C::kSegCopies;
+          const int r = (q / C::kChunks) % kTileRows;
+          int k = ks[0];
+#pragma unroll
+          for (int jj = 1; jj < C::kSegs; ++jj)
+            if (j == jj) k = ks[jj];
+          src_rows[i] = (has_rows && k < kTaps) ? nb[r * kTaps + k] : -1;
+        }
+#pragma unroll
+        for (int i = 0; i < C::kPerThread; ++i) {
+          const int q = pt + i * kProducerThreads;
+          const int j = q / C::kSegCopies;
+          const int r = (q / C::kChunks) % kTileRows;
+          const int sw = (r * C::kRowBytes >> 7) & (C::kChunks - 1);
+          uint8_t* dst = a_st + j * C::kASeg + r * C::kRowBytes + ((chunk_id ^ sw) << 4);
+          // Absent neighbours: source size 0 zero-fills without reading (a
+          // shared zero row would make every SM hit the same L2 line).
+          const __nv_bfloat16* src =
+              src_rows[i] >= 0 ? feats + (int64_t)src_rows[i] * p.cin + c0 + chunk_id * 8 : feats;
+          cp_async_16(dst, src, src_rows[i] >= 0 ? 16u : 0u);
+        }
+        cp_async_arrive_noinc(&full[stage]);
         if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1u;
@@ -318,22 +392,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       *s_abort = 1;
       if (pt == 0) atomicOr(p.status, kStatTimeout);
     }
-    // Drain: wait until every stage this CTA armed has been released by the
-    // MMA warps of all CTAs of the cluster, so that no copy or commit aimed at
-    // this CTA's shared memory is still in flight when it exits.
     cp_async_wait<0>();
-    if (warp == 4) {
-      for (int i = 0; i < C::kStages; ++i) {
-        if (!mbar_wait_for(&empty[stage], phase ^ 1u, ok ? kWaitNs : kDrainNs)) {
-          if (lane == 0) atomicOr(p.status, kStatTimeout);
-          break;
-        }
-        if (++stage == C::kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-    }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
