@@ -188,11 +188,13 @@ sc_handle sc_build_map(const int32_t* coords, int64_t n, int32_t res, void* stre
     m->hash.log2cap = log2cap;
     m->hash.vbits = vbits;
     m->hash.res = res;
+    m->hash.bres = (res + 1) / 2;
     m->hash.bmax = bmax;
     m->hash.n = n;
     m->hash.slots = static_cast<uint64_t*>(dev_alloc(m, cap * sizeof(uint64_t), s));
-    // nbr is padded to whole 128-row tiles (pad rows all -1) so that the
-    // convolution can stage any tile's 13,824-byte block with one bulk copy.
+    // nbr is tile-major [ntiles][27][128] (pad rows -1): a tile's rows are
+    // contiguous per offset, and a tile's whole block (13,824 bytes) is one
+    // contiguous range for the convolution.
     m->nbr = static_cast<int32_t*>(
         dev_alloc(m, (size_t)m->ntiles * sc::kTileRows * sc::kTaps * sizeof(int32_t), s));
     m->tile_mask = static_cast<uint32_t*>(dev_alloc(m, (size_t)m->ntiles * sizeof(uint32_t), s));
@@ -209,7 +211,7 @@ sc_handle sc_build_map(const int32_t* coords, int64_t n, int32_t res, void* stre
     if (e == cudaSuccess) e = sc::launch_hash_insert(coords, m->hash, m->d_status, s);
     if (e == cudaSuccess)
       e = sc::launch_neighbor_query(coords, m->hash, m->nbr, m->tile_mask, m->d_pairs,
-                                    m->d_status, /*pad_tiles=*/true, s);
+                                    m->d_status, sc::kNbrTileMajor, s);
     uint32_t host[4] = {0, 0, 0, 0};
     if (e == cudaSuccess) e = cudaMemcpyAsync(host, m->d_status, 16, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
@@ -286,8 +288,7 @@ sc_status sc_get_neighbor_table(sc_handle h, int32_t* nbr_out, void* stream) {
   if (!is_live(h)) return fail(SC_ERR_BAD_HANDLE, "sc_get_neighbor_table: handle is not live");
   if (h->n == 0) return ok();
   if (!nbr_out) return fail(SC_ERR_INVALID_ARG, "sc_get_neighbor_table: nbr_out is NULL");
-  cudaError_t e = cudaMemcpyAsync(nbr_out, h->nbr, (size_t)h->n * sc::kTaps * sizeof(int32_t),
-                                  cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream));
+  cudaError_t e = sc::launch_nbr_to_row_major(h, nbr_out, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "sc_get_neighbor_table");
   return ok();
 }

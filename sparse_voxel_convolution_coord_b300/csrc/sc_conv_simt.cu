@@ -27,7 +27,11 @@ __global__ void __launch_bounds__(kSimtWarps * 32) k_conv_simt_f32(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t o = (int64_t)blockIdx.x * kSimtWarps + warp;
   if (o >= n) return;  // no block-wide synchronisation below
-  const int32_t nb = lane < kTaps ? __ldg(nbr + o * kTaps + lane) : -1;
+  // tile-major table: row o of tile o / 128, offset k at [tile][k][o % 128]
+  const int32_t nb =
+      lane < kTaps ? __ldg(nbr + (o / kTileRows) * (kTileRows * kTaps) + lane * kTileRows +
+                           (o % kTileRows))
+                   : -1;
   const uint32_t present = __ballot_sync(0xffffffffu, nb >= 0);
   float acc[J];
 #pragma unroll

@@ -104,7 +104,7 @@ struct TcCfg {
 
 struct TcArgs {
   const __nv_bfloat16* feats;  // [n][cin]
-  const int32_t* nbr;          // [ntiles * 128][27], pad rows -1
+  const int32_t* nbr;          // tile-major [ntiles][27][128], pad rows -1
   const uint32_t* tile_mask;   // [ntiles]
   const float* bias;
   float* out;
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + C::kStages * C::kABytes;
-  int32_t* s_nbr = reinterpret_cast<int32_t*>(sB + C::kStages * C::kBBytes);  // [2][128][27]
+  int32_t* s_nbr = reinterpret_cast<int32_t*>(sB + C::kStages * C::kBBytes);  // [2][27][128]
   float* s_bias = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s_nbr) + 2 * kNbrBytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(s_bias + NPAD);
   uint64_t* empty = full + C::kStages;
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int jj = 1; jj < C::kSegs; ++jj)
             if (j == jj) k = ks[jj];
-          src_rows[i] = (has_rows && k < kTaps) ? nb[r * kTaps + k] : -1;
+          src_rows[i] = (has_rows && k < kTaps) ? nb[k * kTileRows + r] : -1;
         }
 #pragma unroll
         for (int i = 0; i < C::kPerThread; ++i) {

@@ -7,16 +7,26 @@
 // the row of the neighbour voxel or -1.  Here:
 //
 //  k_hash_insert     open addressing over a power-of-two table of packed
-//                    64-bit slots (key << vbits | row).  A group of kWindow
-//                    lanes cooperates on one key: it reads a window of
-//                    kWindow consecutive slots in one coalesced load, finds a
-//                    duplicate or the first empty slot with one ballot, and
-//                    claims it with a 64-bit CAS; windows follow linearly.
-//  k_neighbor_query  one thread per voxel; its 26 probes (the centre is the
-//                    voxel itself) are issued together, then resolved.  The
-//                    block's 128 rows x 27 results are staged in shared memory
-//                    and written with coalesced 16-byte stores.  The block
-//                    also ORs its rows' presence masks into the tile mask the
+//                    64-bit slots (key << vbits | row) with brick-local home
+//                    slots and double-hashing probes (sc_internal.cuh).  The
+//                    warp inserts its 32 keys in synchronous probing rounds:
+//                    in each round every lane whose key is still pending
+//                    claims its next probe slot with one 64-bit CAS, and a
+//                    ballot ends the rounds once no lane is pending.  The CAS
+//                    returns the occupant, so a duplicate key is seen when
+//                    its twin's slot is reached.  Errors are OR-reduced per
+//                    warp.
+//  k_neighbor_query  one thread per (voxel, neighbour column dx, dy): the
+//                    three neighbours dz = -1, 0, 1 of the column are probed
+//                    with three independent loads (brick-local homes put a
+//                    warp's loads, 32 consecutive voxels on one column, on
+//                    few cache lines), collisions followed along the probe
+//                    sequence.  Nine threads per voxel keep enough warps in
+//                    flight to hide the probe latency, which one thread per
+//                    voxel with 26 dependent resolutions could not.  The
+//                    tile-major output [tile][27][128] is written coalesced
+//                    (a warp writes 32 consecutive rows of one offset).  Each
+//                    block ORs its rows' presence bits into the tile mask the
 //                    convolution uses to skip absent offsets, and adds its
 //                    pair count to a global counter.
 //  k_pairs_*         CSR pair lists per offset (ascending output row),
@@ -27,136 +37,125 @@
 
 namespace sc {
 
-constexpr int kWindow = 8;  // lanes (and slots) per cooperative probe window
+constexpr int kInsertThreads = 256;
 
 // ---------------------------------------------------------------------------
 // insert
 
-__global__ void __launch_bounds__(256) k_hash_insert(const int4* __restrict__ coords,
-                                                     HashParams hp, uint32_t* status) {
+__global__ void __launch_bounds__(kInsertThreads) k_hash_insert(const int4* __restrict__ coords,
+                                                                HashParams hp, uint32_t* status) {
   const int lane = threadIdx.x & 31;
-  const int glane = lane % kWindow;
-  const int gbase = lane - glane;
-  const unsigned gmask = (kWindow == 32) ? 0xffffffffu : (((1u << kWindow) - 1u) << gbase);
-  const int64_t group = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kWindow;
-  const int64_t ngroups = ((int64_t)gridDim.x * blockDim.x) / kWindow;
-  const uint64_t res = (uint64_t)hp.res;
+  const int64_t i = (int64_t)blockIdx.x * kInsertThreads + threadIdx.x;
+  unsigned long long* slots = reinterpret_cast<unsigned long long*>(hp.slots);
   uint32_t err = 0;
-
-  for (int64_t i = group; i < hp.n; i += ngroups) {
+  bool pending = false;
+  uint64_t key = 0, mine = 0, pos = 0, step = 0;
+  if (i < hp.n) {
     const int4 c = __ldg(coords + i);
-    const bool ok = c.x >= 0 && (unsigned)c.y < (unsigned)hp.res &&
-                    (unsigned)c.z < (unsigned)hp.res && (unsigned)c.w < (unsigned)hp.res;
-    if (!ok) {
+    const bool in_range = c.x >= 0 && (unsigned)c.y < (unsigned)hp.res &&
+                          (unsigned)c.z < (unsigned)hp.res && (unsigned)c.w < (unsigned)hp.res;
+    if (!in_range) {
       err |= kStatRange;
-      continue;
-    }
-    if ((uint64_t)c.x >= hp.bmax) {
+    } else if ((uint64_t)c.x >= hp.bmax) {
       err |= kStatKeySpace;
+    } else {
+      key = cell_key(hp, c.x, c.y, c.z, c.w);
+      mine = (key << hp.vbits) | (uint64_t)i;
+      pos = home_slot(hp, c.x, c.y, c.z, c.w);
+      step = probe_step(hp, key);
+      pending = true;
+    }
+  }
+  // Synchronous probing rounds; at most `capacity` rounds (every slot).
+  for (uint64_t round = 0; __any_sync(0xffffffffu, pending); ++round) {
+    if (!pending) continue;
+    if (round > hp.cap_mask) {
+      err |= kStatTableFull;
+      pending = false;
       continue;
     }
-    const uint64_t key = (((uint64_t)c.x * res + (uint64_t)c.y) * res + (uint64_t)c.z) * res +
-                         (uint64_t)c.w;
-    const uint64_t mine = (key << hp.vbits) | (uint64_t)i;
-    uint64_t pos = hash_home(key, hp.log2cap) & ~(uint64_t)(kWindow - 1);
-    bool done = false;
-    for (uint64_t w = 0; w <= hp.cap_mask / kWindow && !done; ++w) {
-      const uint64_t s = __ldcg(reinterpret_cast<const unsigned long long*>(hp.slots) + pos + glane);
-      const unsigned same = __ballot_sync(gmask, s != kEmptySlot && (s >> hp.vbits) == key) & gmask;
-      if (same) {
-        err |= kStatDuplicate;
-        done = true;
-        break;
-      }
-      unsigned empty = __ballot_sync(gmask, s == kEmptySlot) & gmask;
-      while (empty) {
-        const int leader = __ffs(empty) - 1;
-        unsigned long long old = 0;
-        if (lane == leader)
-          old = atomicCAS(reinterpret_cast<unsigned long long*>(hp.slots) + pos + (leader - gbase),
-                          (unsigned long long)kEmptySlot, (unsigned long long)mine);
-        old = __shfl_sync(gmask, old, leader);
-        if (old == kEmptySlot) {
-          done = true;
-          break;
-        }
-        if ((old >> hp.vbits) == key) {
-          err |= kStatDuplicate;
-          done = true;
-          break;
-        }
-        empty &= ~(1u << leader);
-      }
-      pos = (pos + kWindow) & hp.cap_mask;
+    const unsigned long long old = atomicCAS(slots + pos, kEmptySlot, mine);
+    if (old == kEmptySlot) {
+      pending = false;
+    } else if ((old >> hp.vbits) == key) {
+      err |= kStatDuplicate;
+      pending = false;
+    } else {
+      pos = (pos + step) & hp.cap_mask;
     }
-    if (!done) err |= kStatTableFull;
   }
-  if (err && glane == 0) atomicOr(status, err);
+  err = __reduce_or_sync(0xffffffffu, err);
+  if (err && lane == 0) atomicOr(status, err);
 }
 
 // ---------------------------------------------------------------------------
 // query
 
-// Resolve a key whose first probe (the window start) returned `s`.
-__device__ __forceinline__ int32_t finish_probe(const HashParams& hp, uint64_t key, uint64_t pos,
-                                                uint64_t s) {
+// Row of `key` whose home slot `home` held `s`, continuing its probe
+// sequence; -1 if absent.
+__device__ __forceinline__ int32_t finish_probe(const HashParams& hp, uint64_t key, uint64_t home,
+                                                unsigned long long s) {
   const uint64_t vmask = (1ull << hp.vbits) - 1ull;
-  for (uint64_t it = 0; it <= hp.cap_mask; ++it) {
+  const unsigned long long* slots = reinterpret_cast<const unsigned long long*>(hp.slots);
+  if (s == kEmptySlot) return -1;
+  if ((s >> hp.vbits) == key) return (int32_t)(s & vmask);
+  const uint64_t step = probe_step(hp, key);
+  uint64_t pos = home;
+  for (uint64_t it = 0; it < hp.cap_mask; ++it) {
+    pos = (pos + step) & hp.cap_mask;
+    s = __ldg(slots + pos);
     if (s == kEmptySlot) return -1;
     if ((s >> hp.vbits) == key) return (int32_t)(s & vmask);
-    pos = (pos + 1) & hp.cap_mask;
-    s = __ldg(reinterpret_cast<const unsigned long long*>(hp.slots) + pos);
   }
   return -1;
 }
 
+// Grid (tiles, 9): block (t, col) resolves, for the 128 voxels of tile t,
+// the three neighbours (dz = -1, 0, 1) of neighbour column
+// col = 3 * (dx + 1) + (dy + 1), i.e. offsets k = 3 * col + {0, 1, 2}.
+template <NbrLayout L>
 __global__ void __launch_bounds__(kTileRows) k_neighbor_query(
     const int4* __restrict__ coords, HashParams hp, int32_t* __restrict__ nbr,
-    uint32_t* __restrict__ tile_mask, unsigned long long* pair_count, uint32_t* status,
-    bool pad_tiles) {
-  __shared__ __align__(16) int32_t s_nbr[kTileRows * kTaps];
+    uint32_t* __restrict__ tile_mask, unsigned long long* pair_count) {
   __shared__ uint32_t s_or[kTileRows / 32];
   __shared__ uint32_t s_cnt[kTileRows / 32];
+  const unsigned long long* slots = reinterpret_cast<const unsigned long long*>(hp.slots);
+  const int col = blockIdx.y;
+  const int dx = col / 3 - 1, dy = col % 3 - 1;
   const int64_t row0 = (int64_t)blockIdx.x * kTileRows;
   const int64_t o = row0 + threadIdx.x;
-  uint32_t mask = 0;
-  if (o < hp.n) {
-    const int4 c = __ldg(coords + o);
-    const int64_t res = hp.res;
-    const uint64_t key0 = (((uint64_t)c.x * res + (uint64_t)c.y) * res + (uint64_t)c.z) * res +
-                          (uint64_t)c.w;
-    uint64_t pos[kTaps], s[kTaps];
-    bool inside[kTaps];
+  const bool valid = o < hp.n;
+  const int4 c = valid ? __ldg(coords + o) : make_int4(0, 0, 0, 0);
+  const int x = c.y + dx, y = c.z + dy;
+  const bool colin =
+      valid && (unsigned)x < (unsigned)hp.res && (unsigned)y < (unsigned)hp.res;
+  unsigned long long s[3];
+  uint64_t home[3];
+  bool in[3];
 #pragma unroll
-    for (int k = 0; k < kTaps; ++k) {
-      const int dx = k / 9 - 1, dy = (k / 3) % 3 - 1, dz = k % 3 - 1;
-      inside[k] = (unsigned)(c.y + dx) < (unsigned)hp.res &&
-                  (unsigned)(c.z + dy) < (unsigned)hp.res && (unsigned)(c.w + dz) < (unsigned)hp.res;
-      const uint64_t key = key0 + (uint64_t)((int64_t)dx * res * res + (int64_t)dy * res + dz);
-      pos[k] = hash_home(key, hp.log2cap) & ~(uint64_t)(kWindow - 1);
-      s[k] = (inside[k] && k != kCentre)
-                 ? __ldg(reinterpret_cast<const unsigned long long*>(hp.slots) + pos[k])
-                 : kEmptySlot;
-    }
-#pragma unroll
-    for (int k = 0; k < kTaps; ++k) {
-      const int dx = k / 9 - 1, dy = (k / 3) % 3 - 1, dz = k % 3 - 1;
-      int32_t r;
-      if (k == kCentre) {
-        r = (int32_t)o;
-      } else {
-        const uint64_t key = key0 + (uint64_t)((int64_t)dx * res * res + (int64_t)dy * res + dz);
-        r = inside[k] ? finish_probe(hp, key, pos[k], s[k]) : -1;
-      }
-      s_nbr[threadIdx.x * kTaps + k] = r;
-      mask |= (r >= 0 ? 1u : 0u) << k;
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < kTaps; ++k) s_nbr[threadIdx.x * kTaps + k] = -1;
+  for (int j = 0; j < 3; ++j) {
+    const int z = c.w + j - 1;
+    in[j] = colin && (unsigned)z < (unsigned)hp.res && !(col == 4 && j == 1);
+    home[j] = in[j] ? home_slot(hp, c.x, x, y, z) : 0;
+    s[j] = in[j] ? __ldg(slots + home[j]) : kEmptySlot;
   }
-  const uint32_t wor = __reduce_or_sync(0xffffffffu, mask);
-  const uint32_t wcnt = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(mask));
+  uint32_t bits = 0;
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const int k = 3 * col + j;
+    int32_t r;
+    if (k == kCentre)
+      r = valid ? (int32_t)o : -1;
+    else
+      r = in[j] ? finish_probe(hp, cell_key(hp, c.x, x, y, c.w + j - 1), home[j], s[j]) : -1;
+    bits |= (r >= 0 ? 1u : 0u) << k;
+    if constexpr (L == kNbrTileMajor)
+      nbr[row0 * kTaps + k * kTileRows + threadIdx.x] = r;
+    else if (valid)
+      nbr[o * kTaps + k] = r;
+  }
+  const uint32_t wor = __reduce_or_sync(0xffffffffu, bits);
+  const uint32_t wcnt = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(bits));
   if ((threadIdx.x & 31) == 0) {
     s_or[threadIdx.x >> 5] = wor;
     s_cnt[threadIdx.x >> 5] = wcnt;
@@ -168,49 +167,75 @@ __global__ void __launch_bounds__(kTileRows) k_neighbor_query(
       m |= s_or[w];
       cnt += s_cnt[w];
     }
-    tile_mask[blockIdx.x] = m;
-    atomicAdd(pair_count, (unsigned long long)cnt);
+    if (m) atomicOr(tile_mask + blockIdx.x, m);  // zeroed before the launch
+    if (cnt) atomicAdd(pair_count, (unsigned long long)cnt);
   }
-  const int64_t rows = pad_tiles ? (int64_t)kTileRows : min((int64_t)kTileRows, hp.n - row0);
-  const int total = (int)rows * kTaps;
-  int32_t* dst = nbr + row0 * kTaps;  // 16-byte aligned: row0 * 27 * 4 = blockIdx * 13824
+}
+
+// nbr_out[n][27] from the tile-major table: one block per tile, staged in
+// shared memory so that both sides are coalesced.
+__global__ void __launch_bounds__(kTileRows) k_nbr_to_row_major(const int32_t* __restrict__ nbr_t,
+                                                                int64_t n,
+                                                                int32_t* __restrict__ out) {
+  __shared__ __align__(16) int32_t s[kTileRows * kTaps];
+  const int64_t row0 = (int64_t)blockIdx.x * kTileRows;
+  const int32_t* src = nbr_t + row0 * kTaps;
+#pragma unroll 3
+  for (int k = 0; k < kTaps; ++k) s[threadIdx.x * kTaps + k] = src[k * kTileRows + threadIdx.x];
+  __syncthreads();
+  const int total = (int)min((int64_t)kTileRows, n - row0) * kTaps;
+  int32_t* dst = out + row0 * kTaps;
   const int nvec = total >> 2;
-  for (int i = threadIdx.x; i < nvec; i += kTileRows)
-    reinterpret_cast<int4*>(dst)[i] = reinterpret_cast<const int4*>(s_nbr)[i];
-  for (int i = (nvec << 2) + threadIdx.x; i < total; i += kTileRows) dst[i] = s_nbr[i];
-  (void)status;
+  if ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+    for (int i = threadIdx.x; i < nvec; i += kTileRows)
+      reinterpret_cast<int4*>(dst)[i] = reinterpret_cast<const int4*>(s)[i];
+    for (int i = (nvec << 2) + threadIdx.x; i < total; i += kTileRows) dst[i] = s[i];
+  } else {
+    for (int i = threadIdx.x; i < total; i += kTileRows) dst[i] = s[i];
+  }
 }
 
 cudaError_t launch_hash_insert(const int32_t* coords, const HashParams& hp, uint32_t* status,
                                cudaStream_t s) {
   if (hp.n == 0) return cudaSuccess;
-  const int64_t threads = hp.n * kWindow;
-  const int64_t blocks = std::min<int64_t>((threads + 255) / 256, 148LL * 64);
-  k_hash_insert<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const int4*>(coords), hp,
-                                                  status);
+  const int64_t blocks = (hp.n + kInsertThreads - 1) / kInsertThreads;
+  k_hash_insert<<<(unsigned)blocks, kInsertThreads, 0, s>>>(reinterpret_cast<const int4*>(coords),
+                                                            hp, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_neighbor_query(const int32_t* coords, const HashParams& hp, int32_t* nbr,
                                   uint32_t* tile_mask, unsigned long long* pair_count,
-                                  uint32_t* status, bool pad_tiles, cudaStream_t s) {
+                                  uint32_t* status, NbrLayout layout, cudaStream_t s) {
+  (void)status;
   if (hp.n == 0) return cudaSuccess;
-  const int64_t blocks = (hp.n + kTileRows - 1) / kTileRows;
-  k_neighbor_query<<<(unsigned)blocks, kTileRows, 0, s>>>(
-      reinterpret_cast<const int4*>(coords), hp, nbr, tile_mask, pair_count, status, pad_tiles);
+  const int64_t tiles = (hp.n + kTileRows - 1) / kTileRows;
+  const int4* c4 = reinterpret_cast<const int4*>(coords);
+  cudaError_t e = cudaMemsetAsync(tile_mask, 0, (size_t)tiles * sizeof(uint32_t), s);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)tiles, 9);
+  if (layout == kNbrTileMajor)
+    k_neighbor_query<kNbrTileMajor><<<grid, kTileRows, 0, s>>>(c4, hp, nbr, tile_mask, pair_count);
+  else
+    k_neighbor_query<kNbrRowMajor><<<grid, kTileRows, 0, s>>>(c4, hp, nbr, tile_mask, pair_count);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nbr_to_row_major(const sc_map* m, int32_t* nbr_out, cudaStream_t s) {
+  if (m->n == 0) return cudaSuccess;
+  k_nbr_to_row_major<<<(unsigned)m->ntiles, kTileRows, 0, s>>>(m->nbr, m->n, nbr_out);
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
 // pair lists (CSR per offset, ascending output row within an offset)
 
-__global__ void __launch_bounds__(kTileRows) k_pairs_count(const int32_t* __restrict__ nbr,
-                                                           int64_t n, int64_t nblocks,
+__global__ void __launch_bounds__(kTileRows) k_pairs_count(const int32_t* __restrict__ nbr_t,
+                                                           int64_t nblocks,
                                                            int64_t* __restrict__ counts) {
-  const int64_t o = (int64_t)blockIdx.x * kTileRows + threadIdx.x;
+  const int32_t* col = nbr_t + (int64_t)blockIdx.x * kTileRows * kTaps + threadIdx.x;
   for (int k = 0; k < kTaps; ++k) {
-    const bool p = o < n && nbr[o * kTaps + k] >= 0;
-    const int c = __syncthreads_count(p);
+    const int c = __syncthreads_count(col[k * kTileRows] >= 0);  // pad rows are -1
     if (threadIdx.x == 0) counts[(int64_t)k * nblocks + blockIdx.x] = c;
   }
 }
@@ -254,15 +279,16 @@ __global__ void __launch_bounds__(1024) k_scan_exclusive(int64_t* data, int64_t 
   if (threadIdx.x == 0) total[0] = s_carry;
 }
 
-__global__ void __launch_bounds__(kTileRows) k_pairs_write(const int32_t* __restrict__ nbr,
-                                                           int64_t n, int64_t nblocks,
+__global__ void __launch_bounds__(kTileRows) k_pairs_write(const int32_t* __restrict__ nbr_t,
+                                                           int64_t nblocks,
                                                            const int64_t* __restrict__ offs,
                                                            int32_t* pin, int32_t* pout) {
   __shared__ int s_warp[kTileRows / 32];
   const int64_t o = (int64_t)blockIdx.x * kTileRows + threadIdx.x;
+  const int32_t* col = nbr_t + (int64_t)blockIdx.x * kTileRows * kTaps + threadIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int k = 0; k < kTaps; ++k) {
-    const int32_t i = o < n ? nbr[o * kTaps + k] : -1;
+    const int32_t i = col[k * kTileRows];
     const bool p = i >= 0;
     const unsigned b = __ballot_sync(0xffffffffu, p);
     if (lane == 0) s_warp[warp] = __popc(b);
@@ -292,15 +318,14 @@ size_t pairs_scratch_bytes(int64_t n) {
 
 cudaError_t launch_pairs(const sc_map* m, int64_t* off_host, int32_t* in, int32_t* out,
                          void* scratch, cudaStream_t s) {
-  const int64_t n = m->n;
-  const int64_t nblocks = (n + kTileRows - 1) / kTileRows;
+  const int64_t nblocks = m->ntiles;
   int64_t* counts = static_cast<int64_t*>(scratch);
   int64_t* total = counts + kTaps * nblocks;
   int64_t* off28 = total + 1;
-  k_pairs_count<<<(unsigned)nblocks, kTileRows, 0, s>>>(m->nbr, n, nblocks, counts);
+  k_pairs_count<<<(unsigned)nblocks, kTileRows, 0, s>>>(m->nbr, nblocks, counts);
   k_scan_exclusive<<<1, 1024, 0, s>>>(counts, kTaps * nblocks, total);
   if (in || out)
-    k_pairs_write<<<(unsigned)nblocks, kTileRows, 0, s>>>(m->nbr, n, nblocks, counts, in, out);
+    k_pairs_write<<<(unsigned)nblocks, kTileRows, 0, s>>>(m->nbr, nblocks, counts, in, out);
   k_pairs_offsets<<<1, 32, 0, s>>>(counts, nblocks, total, off28);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

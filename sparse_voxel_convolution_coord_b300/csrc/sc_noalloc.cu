@@ -101,6 +101,7 @@ extern "C" SC_API sc_status sc_build_neighbor_table_noalloc(const int32_t* coord
   hp.log2cap = log2cap;
   hp.vbits = vbits;
   hp.res = res;
+  hp.bres = (res + 1) / 2;
   hp.bmax = bmax;
   hp.n = n;
   uint32_t* tile_mask = reinterpret_cast<uint32_t*>(scratch + kMaskWordOffset);
@@ -115,7 +116,7 @@ extern "C" SC_API sc_status sc_build_neighbor_table_noalloc(const int32_t* coord
   if (e == cudaSuccess) e = sc::launch_hash_insert(coords, hp, status, s);
   if (e == cudaSuccess)
     e = sc::launch_neighbor_query(coords, hp, nbr_out, tile_mask, pair_count, status,
-                                  /*pad_tiles=*/false, s);
+                                  sc::kNbrRowMajor, s);
   uint32_t host[4] = {0, 0, 0, 0};
   if (e == cudaSuccess) e = cudaMemcpyAsync(host, status, 16, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
