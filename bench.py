@@ -33,7 +33,7 @@ FLUSH_BYTES = 256 << 20
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -209,6 +209,38 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # our arm
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
+# of the convolution kernel, from the ncu capture summarised in profiles/,
+# valid only for the kernel source it was measured on (sha1 of the file).
+MEASURED_TRAFFIC = {
+    # workload name: (sha1 of sc_conv_tc.cu, bytes per launch)
+    "sq3x64_30k_c256_bf16": ("39de549d4fae4f08ea5a6e81687dc7a11949809b", 22143232 + 73216),
+}
+
+
+def _file_sha1(path):
+    import hashlib
+    return hashlib.sha1(open(path, "rb").read()).hexdigest()
+
+
+def time_forward_alone(sc, torch, m, feats, weight, bias, out, flush, stream, reps=200):
+    """Median device time of one forward launch: the stream is first held by a
+    GPU sleep so that every (flush, event, forward, event) group is queued
+    before the GPU reaches it (no host gaps inside the events); L2 is flushed
+    before each launch."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(5e7))
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        sc.sc_forward(m, feats, weight, bias, out)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs[10:])
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
@@ -223,6 +255,7 @@ def run_ours(args):
     p = synth.make_problem(args.config)
     cin, cout = p.feats.shape[1], p.weight.shape[2]
     tdt = torch.bfloat16 if p.config.dtype == "bf16" else torch.float32
+    esize = 2 if p.config.dtype == "bf16" else 4
     coords = torch.from_numpy(p.coords).to(dev)
     feats = torch.from_numpy(p.feats).to(dev).to(tdt)
     weight = torch.from_numpy(p.weight).to(dev).to(tdt)
@@ -235,7 +268,11 @@ def run_ours(args):
     pairs = m.pairs
     m.free()
     flops = 2.0 * pairs * cin * cout
+    # algorithmic bytes (every byte the path must move once)
+    fwd_bytes = p.n * cin * esize + 108 * p.n + 4 * p.n * cout + 27 * cin * cout * esize
+    build_bytes = 132 * p.n  # coords 16N + one slot write 8N + neighbour table 108N
 
+    # -- the timed step: map build + forward, L2 flushed before each step
     def step(evs=None):
         if evs is not None:
             evs[0].record(stream)
@@ -270,24 +307,19 @@ def run_ours(args):
     build_ms = [e[0].elapsed_time(e[1]) for e in evs]
     fwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
     t_step = sum(step_ms) / K
-    t_fwd = sum(fwd_ms) / K
     t_build = sum(build_ms) / K
+    t_fwd = sum(fwd_ms) / K
     t_step_max = max_over_ranks(dist, t_step)
 
-    # forward kernel alone (no host gap before its launch): events around back-to-back
-    # forwards on one map, L2 flushed between them
+    # -- the convolution kernel alone (roofline), on one map
     mp = sc.sc_build_map(coords, p.res)
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(200)]
-    for i in range(200):
-        flush.zero_()
-        kev[i][0].record(stream)
+    for _ in range(5):
         sc.sc_forward(mp, feats, weight, bias, out)
-        kev[i][1].record(stream)
-    torch.cuda.synchronize()
-    t_kernel = statistics.median(a.elapsed_time(b) for a, b in kev[20:])
+    t_kernel = time_forward_alone(sc, torch, mp, feats, weight, bias, out, flush, stream)
+    sc.sc_device_status(mp)
     mp.free()
 
-    # end to end through the public API from pinned host buffers
+    # -- end to end through the public API from pinned host buffers
     h_coords = torch.from_numpy(p.coords).pin_memory()
     h_feats = torch.from_numpy(p.feats).to(tdt).pin_memory()
     h_weight = torch.from_numpy(p.weight).to(tdt).pin_memory()
@@ -325,7 +357,30 @@ def run_ours(args):
     t_e2e = max_over_ranks(dist, e0.elapsed_time(e1) / KE)
 
     peaks = load_peaks()
-    achieved = flops / (t_kernel * 1e-3) / 1e12
+    conv_src = os.path.join(ROOT, "sparse_voxel_convolution_coord_b300", "csrc", "sc_conv_tc.cu")
+    traffic = None
+    rec = MEASURED_TRAFFIC.get(p.config.name)
+    if rec is not None and p.config.dtype == "bf16" and rec[0] == _file_sha1(conv_src):
+        traffic = rec[1]
+    if p.config.dtype == "bf16":
+        achieved = flops / (t_kernel * 1e-3) / 1e12
+        roofline = {"kernel": "k_conv_tc (gather-implicit-GEMM, tcgen05, bf16 -> fp32 TMEM)",
+                    "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                    "frac_of_sustained": (achieved / peaks["bf16_tflops_sustained"]
+                                          if peaks.get("bf16_tflops_sustained") else None),
+                    "peak_source": peaks["source"] + " bf16 burst (MEASURED_PEAKS.json)",
+                    "traffic": traffic, "kernel_us": t_kernel * 1e3,
+                    "algorithmic_flops_per_launch": flops,
+                    "algorithmic_bytes_per_launch": fwd_bytes}
+    else:
+        gbs = fwd_bytes / (t_kernel * 1e-3) / 1e9
+        roofline = {"kernel": "k_conv_simt_f32 (fp32 FFMA gather-GEMM)", "bound": "hbm",
+                    "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"] + " hbm",
+                    "traffic": None, "kernel_us": t_kernel * 1e3,
+                    "algorithmic_bytes_per_launch": fwd_bytes}
+    build_gbs = build_bytes / (t_build * 1e-3) / 1e9
     line = {
         "metric": METRIC,
         "value": world * flops / (t_step_max * 1e-3) / 1e12,
@@ -334,26 +389,23 @@ def run_ours(args):
         "ms_per_step": t_step_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if p.config.dtype == "bf16" else "f32",
-        "data": "synthetic",
+        "data": "synthetic (seeded superquadric voxel shells; random N(0,1) features, "
+                "N(0, 1/sqrt(27 cin)) weights)",
         "config": {"workload": p.config.name, "description": p.config.description,
                    "n_voxels": p.n, "pairs": pairs, "cin": cin, "cout": cout, "res": p.res,
                    "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "flushed before every timed step (256 MB write, outside the step events)"},
+                   "l2": "flushed before every timed step (256 MB write, outside the events)"},
         "voxels_per_s": world * p.n / (t_step_max * 1e-3),
-        "breakdown_ms": {"build_map": t_build, "forward_in_step": t_fwd,
+        "breakdown_ms": {"build_map_incl_host_sync": t_build, "forward_in_step": t_fwd,
                          "forward_kernel_alone": t_kernel,
                          "wall_per_step_incl_flush": wall / K * 1e3},
-        "roofline": {"kernel": "k_conv_tc (gather-implicit-GEMM, tcgen05)", "bound": "tensor",
-                     "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16_tflops"],
-                     "frac_of_sustained": (achieved / peaks["bf16_tflops_sustained"]
-                                           if peaks.get("bf16_tflops_sustained") else None),
-                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json burst)",
-                     "traffic": None,
-                     "algorithmic_flops_per_launch": flops},
+        "roofline": roofline,
+        "map_build": {"bound": "hbm", "algorithmic_bytes": build_bytes,
+                      "achieved_gbs_incl_host_sync": build_gbs,
+                      "frac_of_hbm": build_gbs / peaks["hbm_gbs"]},
         "e2e": {"value": world * flops / (t_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": t_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * K,
+        "gpu_launches": 3 * K,  # per step: k_hash_insert, k_neighbor_query, one conv kernel
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

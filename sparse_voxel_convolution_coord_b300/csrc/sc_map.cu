@@ -129,6 +129,17 @@ __global__ void __launch_bounds__(kTileRows) k_neighbor_query(
   const int x = c.y + dx, y = c.z + dy;
   const bool colin =
       valid && (unsigned)x < (unsigned)hp.res && (unsigned)y < (unsigned)hp.res;
+  // Shared arithmetic of the column: the key of (x, y, z - 1) (the other two
+  // are +1, +2) and the groups of the two bricks along z that the three
+  // cells fall in (bricks zb and zb + 1, zb = (z - 1) >> 1).
+  const int zb = (c.w - 1) >> 1;
+  const uint64_t key_lo = cell_key(hp, c.x, x, y, c.w - 1);
+  const int64_t BR = hp.bres;
+  const int64_t brick_lo = (((int64_t)c.x * BR + (x >> 1)) * BR + (y >> 1)) * BR + zb;
+  const int gshift = 64 - (hp.log2cap - 3);
+  const uint64_t g_lo = ((uint64_t)brick_lo * 0x9E3779B97F4A7C15ull) >> gshift;
+  const uint64_t g_hi = ((uint64_t)(brick_lo + 1) * 0x9E3779B97F4A7C15ull) >> gshift;
+  const uint64_t cellxy = (uint64_t)(((x & 1) << 2) | ((y & 1) << 1));
   unsigned long long s[3];
   uint64_t home[3];
   bool in[3];
@@ -136,7 +147,7 @@ __global__ void __launch_bounds__(kTileRows) k_neighbor_query(
   for (int j = 0; j < 3; ++j) {
     const int z = c.w + j - 1;
     in[j] = colin && (unsigned)z < (unsigned)hp.res && !(col == 4 && j == 1);
-    home[j] = in[j] ? home_slot(hp, c.x, x, y, z) : 0;
+    home[j] = ((((z >> 1) != zb) ? g_hi : g_lo) << 3) | cellxy | (uint64_t)(z & 1);
     s[j] = in[j] ? __ldg(slots + home[j]) : kEmptySlot;
   }
   uint32_t bits = 0;
@@ -147,7 +158,7 @@ __global__ void __launch_bounds__(kTileRows) k_neighbor_query(
     if (k == kCentre)
       r = valid ? (int32_t)o : -1;
     else
-      r = in[j] ? finish_probe(hp, cell_key(hp, c.x, x, y, c.w + j - 1), home[j], s[j]) : -1;
+      r = in[j] ? finish_probe(hp, key_lo + (uint64_t)j, home[j], s[j]) : -1;
     bits |= (r >= 0 ? 1u : 0u) << k;
     if constexpr (L == kNbrTileMajor)
       nbr[row0 * kTaps + k * kTileRows + threadIdx.x] = r;
