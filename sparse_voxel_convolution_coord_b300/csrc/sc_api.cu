@@ -102,10 +102,8 @@ void dev_free(sc_map* m, void* p, cudaStream_t s) {
 }
 
 void release_buffers(sc_map* m, cudaStream_t s) {
-  dev_free(m, m->hash.slots, s);
-  dev_free(m, m->nbr, s);
-  dev_free(m, m->tile_mask, s);
-  dev_free(m, m->d_status, s);
+  dev_free(m, m->block, s);
+  m->block = nullptr;
   m->hash.slots = nullptr;
   m->nbr = nullptr;
   m->tile_mask = nullptr;
@@ -191,23 +189,28 @@ sc_handle sc_build_map(const int32_t* coords, int64_t n, int32_t res, void* stre
     m->hash.bres = (res + 1) / 2;
     m->hash.bmax = bmax;
     m->hash.n = n;
-    m->hash.slots = static_cast<uint64_t*>(dev_alloc(m, cap * sizeof(uint64_t), s));
-    // nbr is tile-major [ntiles][27][128] (pad rows -1): a tile's rows are
-    // contiguous per offset, and a tile's whole block (13,824 bytes) is one
-    // contiguous range for the convolution.
-    m->nbr = static_cast<int32_t*>(
-        dev_alloc(m, (size_t)m->ntiles * sc::kTileRows * sc::kTaps * sizeof(int32_t), s));
-    m->tile_mask = static_cast<uint32_t*>(dev_alloc(m, (size_t)m->ntiles * sizeof(uint32_t), s));
-    m->d_status = static_cast<uint32_t*>(dev_alloc(m, 16, s));
-    if (!m->hash.slots || !m->nbr || !m->tile_mask || !m->d_status) {
-      release_buffers(m, s);
+    // One allocation, carved (every piece 256-byte aligned): the hash table,
+    // the tile-major neighbour table [ntiles][27][128] (pad rows -1: a
+    // tile's rows are contiguous per offset, and a tile's whole 13,824-byte
+    // block is one contiguous range for the convolution), the tile masks and
+    // the 16-byte status / pair-count block.
+    auto up = [](size_t b) { return (b + 255) & ~size_t(255); };
+    const size_t b_slots = up(cap * sizeof(uint64_t));
+    const size_t b_nbr = up((size_t)m->ntiles * sc::kTileRows * sc::kTaps * sizeof(int32_t));
+    const size_t b_mask = up((size_t)m->ntiles * sizeof(uint32_t));
+    m->block = dev_alloc(m, b_slots + b_nbr + b_mask + 256, s);
+    if (!m->block) {
       delete m;
       fail(SC_ERR_ALLOC, "sc_build_map: device allocation failed (n=%lld)", (long long)n);
       return nullptr;
     }
+    uint8_t* base = static_cast<uint8_t*>(m->block);
+    m->hash.slots = reinterpret_cast<uint64_t*>(base);
+    m->nbr = reinterpret_cast<int32_t*>(base + b_slots);
+    m->tile_mask = reinterpret_cast<uint32_t*>(base + b_slots + b_nbr);
+    m->d_status = reinterpret_cast<uint32_t*>(base + b_slots + b_nbr + b_mask);
     m->d_pairs = reinterpret_cast<unsigned long long*>(m->d_status + 2);
-    cudaError_t e = cudaMemsetAsync(m->hash.slots, 0xFF, cap * sizeof(uint64_t), s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(m->d_status, 0, 16, s);
+    cudaError_t e = sc::launch_map_init(m->hash, m->tile_mask, m->ntiles, m->d_status, s);
     if (e == cudaSuccess) e = sc::launch_hash_insert(coords, m->hash, m->d_status, s);
     if (e == cudaSuccess)
       e = sc::launch_neighbor_query(coords, m->hash, m->nbr, m->tile_mask, m->d_pairs,

@@ -6,17 +6,27 @@
 // accumulation, bias in the same pass).  Used for fp32 inputs, where a
 // tensor-core tf32 product would round the inputs to 10 mantissa bits.
 //
-// One warp owns one output row and all cout columns (lane l holds columns
-// l, l+32, ...).  Per 32-channel slice of the input, the warp first issues
-// the 27 gathers of its neighbour rows together (independent loads, one
-// coalesced 128-byte row slice each) into shared memory, then accumulates
-// over the present offsets with W read through L1 (every warp of the grid
-// reads the same W).  Each output row is written once, no atomics.
+// A block owns 8 output rows (one warp each; lane l holds columns l, l+32,
+// ...).  Per 32-channel slice of the input: every warp gathers its row's 27
+// neighbour slices at once (independent coalesced loads) into shared memory;
+// then, for each offset present in any of the block's rows, the W[k] slice
+// (32 rows x cout) is staged in shared memory by cp.async, double-buffered one
+// offset ahead, and shared by the 8 warps.  Each output row is written once,
+// no atomics.
 #include "sc_internal.cuh"
 
 namespace sc {
 
 constexpr int kSimtWarps = 8;  // output rows per block
+
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_16_ca(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
 
 template <int J>  // columns per lane = J, cout <= 32 * J
 __global__ void __launch_bounds__(kSimtWarps * 32) k_conv_simt_f32(
@@ -24,64 +34,116 @@ __global__ void __launch_bounds__(kSimtWarps * 32) k_conv_simt_f32(
     const float* __restrict__ w, const float* __restrict__ bias, float* __restrict__ out, int cin,
     int cout) {
   __shared__ float s_a[kSimtWarps][kTaps][32];
+  __shared__ uint32_t s_mask[kSimtWarps];
+  extern __shared__ __align__(16) float s_w[];  // [2][32][32 * J]
+  constexpr int kWStride = 32 * J;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t o = (int64_t)blockIdx.x * kSimtWarps + warp;
-  if (o >= n) return;  // no block-wide synchronisation below
+  const bool valid = o < n;
   // tile-major table: row o of tile o / 128, offset k at [tile][k][o % 128]
   const int32_t nb =
-      lane < kTaps ? __ldg(nbr + (o / kTileRows) * (kTileRows * kTaps) + lane * kTileRows +
-                           (o % kTileRows))
-                   : -1;
+      (valid && lane < kTaps)
+          ? __ldg(nbr + (o / kTileRows) * (kTileRows * kTaps) + lane * kTileRows + (o % kTileRows))
+          : -1;
   const uint32_t present = __ballot_sync(0xffffffffu, nb >= 0);
+  if (lane == 0) s_mask[warp] = present;
+  __syncthreads();
+  uint32_t bmask = 0;
+#pragma unroll
+  for (int q = 0; q < kSimtWarps; ++q) bmask |= s_mask[q];
+  const bool vec = (cout & 3) == 0;  // 16-byte copies of W rows
+
   float acc[J];
 #pragma unroll
   for (int j = 0; j < J; ++j) acc[j] = 0.f;
 
+  // Stage W[k][ci0 .. ci0 + width)[0 .. cout) into buffer b.
+  auto stage_w = [&](int k, int ci0, int width, int b) {
+    float* dst = s_w + b * 32 * kWStride;
+    const float* src = w + ((int64_t)k * cin + ci0) * cout;
+    if (vec) {
+      const int per_row = cout >> 2;
+      for (int e = threadIdx.x; e < width * per_row; e += kSimtWarps * 32) {
+        const int r = e / per_row, c4 = e - r * per_row;
+        cp_async_16_ca(dst + r * kWStride + 4 * c4, src + (int64_t)r * cout + 4 * c4);
+      }
+    } else {
+      for (int e = threadIdx.x; e < width * cout; e += kSimtWarps * 32) {
+        const int r = e / cout, c = e - r * cout;
+        cp_async_4(dst + r * kWStride + c, src + (int64_t)r * cout + c);
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+
   for (int ci0 = 0; ci0 < cin; ci0 += 32) {
     const int width = min(32, cin - ci0);
+    uint32_t rem = bmask;
+    if (rem) stage_w(__ffs(rem) - 1, ci0, width, 0);
 #pragma unroll
     for (int k = 0; k < kTaps; ++k) {
       const int32_t i = __shfl_sync(0xffffffffu, nb, k);
       s_a[warp][k][lane] =
           (i >= 0 && lane < width) ? __ldg(feats + (int64_t)i * cin + ci0 + lane) : 0.f;
     }
-    __syncwarp();
-    for (uint32_t rem = present; rem; rem &= rem - 1u) {
+    int buf = 0;
+    while (rem) {
       const int k = __ffs(rem) - 1;
-      const float* wk = w + ((int64_t)k * cin + ci0) * cout + lane;
-#pragma unroll 4
+      rem &= rem - 1u;
+      if (rem) {
+        stage_w(__ffs(rem) - 1, ci0, width, buf ^ 1);
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+      } else {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+      }
+      __syncthreads();  // W slice k and every warp's gathered rows are in place
+      const float* ws = s_w + buf * 32 * kWStride + lane;
+#pragma unroll 8
       for (int cc = 0; cc < width; ++cc) {
         const float a = s_a[warp][k][cc];
-        const float* wr = wk + (int64_t)cc * cout;
 #pragma unroll
         for (int j = 0; j < J; ++j)
-          if (lane + 32 * j < cout) acc[j] = fmaf(a, __ldg(wr + 32 * j), acc[j]);
+          if (lane + 32 * j < cout) acc[j] = fmaf(a, ws[cc * kWStride + 32 * j], acc[j]);
       }
+      __syncthreads();  // buffer buf is free for the offset after next
+      buf ^= 1;
     }
-    __syncwarp();
+    __syncthreads();  // s_a is rewritten for the next slice
   }
+  if (valid) {
 #pragma unroll
-  for (int j = 0; j < J; ++j) {
-    const int c = lane + 32 * j;
-    if (c < cout) out[o * cout + c] = acc[j] + (bias ? __ldg(bias + c) : 0.f);
+    for (int j = 0; j < J; ++j) {
+      const int c = lane + 32 * j;
+      if (c < cout) out[o * cout + c] = acc[j] + (bias ? __ldg(bias + c) : 0.f);
+    }
   }
+}
+
+template <int J>
+cudaError_t launch_simt(const sc_map* m, const float* feats, const float* w, const float* bias,
+                        float* out, int cin, int cout, cudaStream_t s) {
+  const size_t smem = 2ull * 32 * 32 * J * sizeof(float);
+  static bool attr = false;  // opt-in above 48 KB of dynamic shared memory
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_conv_simt_f32<J>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const unsigned blocks = (unsigned)((m->n + kSimtWarps - 1) / kSimtWarps);
+  k_conv_simt_f32<J><<<blocks, kSimtWarps * 32, smem, s>>>(m->nbr, m->n, feats, w, bias, out, cin,
+                                                           cout);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_conv_simt_f32(const sc_map* m, const float* feats, const float* w,
                                  const float* bias, float* out, int cin, int cout,
                                  cudaStream_t s) {
-  const unsigned blocks = (unsigned)((m->n + kSimtWarps - 1) / kSimtWarps);
   const int J = (cout + 31) / 32;
-  const dim3 block(kSimtWarps * 32);
-  if (J <= 1)
-    k_conv_simt_f32<1><<<blocks, block, 0, s>>>(m->nbr, m->n, feats, w, bias, out, cin, cout);
-  else if (J <= 2)
-    k_conv_simt_f32<2><<<blocks, block, 0, s>>>(m->nbr, m->n, feats, w, bias, out, cin, cout);
-  else if (J <= 4)
-    k_conv_simt_f32<4><<<blocks, block, 0, s>>>(m->nbr, m->n, feats, w, bias, out, cin, cout);
-  else
-    k_conv_simt_f32<8><<<blocks, block, 0, s>>>(m->nbr, m->n, feats, w, bias, out, cin, cout);
-  return cudaGetLastError();
+  if (J <= 1) return launch_simt<1>(m, feats, w, bias, out, cin, cout, s);
+  if (J <= 2) return launch_simt<2>(m, feats, w, bias, out, cin, cout, s);
+  if (J <= 4) return launch_simt<4>(m, feats, w, bias, out, cin, cout, s);
+  return launch_simt<8>(m, feats, w, bias, out, cin, cout, s);
 }
 
 }  // namespace sc

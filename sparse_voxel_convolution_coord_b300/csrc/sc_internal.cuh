@@ -329,6 +329,7 @@ struct sc_map {
   int32_t* nbr;          // tile-major [ntiles][27][128], pad rows -1
   uint32_t* tile_mask;   // [ntiles] OR of the 27-bit presence masks of a tile's rows
   uint32_t* d_status;    // device status word + pair counter scratch
+  void* block;           // the one device allocation the buffers above are carved from
   unsigned long long* d_pairs;
   void* (*alloc)(size_t, void*, void*);
   void (*free_fn)(void*, void*, void*);
@@ -337,6 +338,10 @@ struct sc_map {
 
 namespace sc {
 
+// Clear a map's scratch: all slots empty, tile masks and the 16-byte status
+// block zero (slots 16-byte aligned).
+cudaError_t launch_map_init(const HashParams& hp, uint32_t* tile_mask, int64_t ntiles,
+                            uint32_t* status, cudaStream_t s);
 cudaError_t launch_hash_insert(const int32_t* coords, const HashParams& hp, uint32_t* status,
                                cudaStream_t s);
 cudaError_t launch_neighbor_query(const int32_t* coords, const HashParams& hp, int32_t* nbr,

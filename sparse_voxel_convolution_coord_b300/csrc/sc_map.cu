@@ -206,6 +206,29 @@ __global__ void __launch_bounds__(kTileRows) k_nbr_to_row_major(const int32_t* _
   }
 }
 
+// One launch instead of three memsets: every slot empty (all ones), the
+// tile masks and the 16-byte status / pair-count block zero.
+__global__ void __launch_bounds__(256) k_map_init(ulonglong2* __restrict__ slots, int64_t npairs2,
+                                                  uint32_t* __restrict__ tile_mask, int64_t ntiles,
+                                                  uint32_t* __restrict__ status) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const ulonglong2 ones = make_ulonglong2(kEmptySlot, kEmptySlot);
+  for (int64_t i = t; i < npairs2; i += stride) slots[i] = ones;
+  for (int64_t i = t; i < ntiles; i += stride) tile_mask[i] = 0u;
+  if (t < 4) status[t] = 0u;
+}
+
+cudaError_t launch_map_init(const HashParams& hp, uint32_t* tile_mask, int64_t ntiles,
+                            uint32_t* status, cudaStream_t s) {
+  const int64_t npairs2 = (int64_t)(hp.cap_mask + 1) / 2;  // 16-byte stores
+  const int64_t work = std::max<int64_t>(npairs2, ntiles);
+  const int64_t blocks = std::min<int64_t>((work + 255) / 256, 148LL * 8);
+  k_map_init<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, s>>>(
+      reinterpret_cast<ulonglong2*>(hp.slots), npairs2, tile_mask, ntiles, status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_hash_insert(const int32_t* coords, const HashParams& hp, uint32_t* status,
                                cudaStream_t s) {
   if (hp.n == 0) return cudaSuccess;
@@ -222,8 +245,6 @@ cudaError_t launch_neighbor_query(const int32_t* coords, const HashParams& hp, i
   if (hp.n == 0) return cudaSuccess;
   const int64_t tiles = (hp.n + kTileRows - 1) / kTileRows;
   const int4* c4 = reinterpret_cast<const int4*>(coords);
-  cudaError_t e = cudaMemsetAsync(tile_mask, 0, (size_t)tiles * sizeof(uint32_t), s);
-  if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)tiles, 9);
   if (layout == kNbrTileMajor)
     k_neighbor_query<kNbrTileMajor><<<grid, kTileRows, 0, s>>>(c4, hp, nbr, tile_mask, pair_count);

@@ -111,8 +111,8 @@ extern "C" SC_API sc_status sc_build_neighbor_table_noalloc(const int32_t* coord
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The scratch keeps the previous call's contents: clear the slots in use and
   // the status / pair-count words.
-  e = cudaMemsetAsync(scratch, 0xFF, cap * sizeof(uint64_t), s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, 16, s);
+  const int64_t ntiles = (n + sc::kTileRows - 1) / sc::kTileRows;
+  e = sc::launch_map_init(hp, tile_mask, ntiles, status, s);
   if (e == cudaSuccess) e = sc::launch_hash_insert(coords, hp, status, s);
   if (e == cudaSuccess)
     e = sc::launch_neighbor_query(coords, hp, nbr_out, tile_mask, pair_count, status,
