@@ -1,0 +1,68 @@
+"""The N > 1 path of bench.py on CPU: two gloo ranks on 127.0.0.1.
+
+The hot path does not shard across GPUs in this library (replicas only): each
+rank runs the whole workload on its own GPU, ranks meet at a barrier around
+the timed steps, the step time is the maximum over ranks, and the reported
+rate is all ranks' units over that time.  These host-side pieces are what a
+multi-GPU run adds, and they run here without a GPU.
+"""
+import os
+import socket
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, results):
+    import sys
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    r, w, local = bench.dist_env()
+    d = bench.init_dist(w)
+    try:
+        bench.barrier(d)
+        # each rank reports its own step time; the job takes the slowest
+        t_ms = 1.0 + rank            # rank 0: 1 ms, rank 1: 2 ms
+        t_max = bench.max_over_ranks(d, t_ms)
+        rate = bench.whole_job_rate(w, 1000.0, t_max)
+        bench.barrier(d)
+        results[rank] = (r, w, local, t_max, rate)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_max_time_and_whole_job_rate():
+    world = 2
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        results = mgr.dict()
+        mp.start_processes(_rank_main, args=(world, _free_port(), results), nprocs=world,
+                           join=True, start_method="spawn")
+        got = dict(results)
+    assert sorted(got) == [0, 1]
+    for rank, (r, w, local, t_max, rate) in got.items():
+        assert (r, w, local) == (rank, world, rank)
+        assert t_max == pytest.approx(2.0)                    # the slowest rank
+        assert rate == pytest.approx(2 * 1000.0 / 2.0e-3)     # all ranks' units / max time
+
+
+def test_single_rank_needs_no_process_group():
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.init_dist(1) is None
+    assert bench.max_over_ranks(None, 3.5) == 3.5
+    assert bench.whole_job_rate(1, 10.0, 5.0) == pytest.approx(2000.0)
