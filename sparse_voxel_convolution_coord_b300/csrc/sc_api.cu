@@ -198,7 +198,7 @@ sc_handle sc_build_map(const int32_t* coords, int64_t n, int32_t res, void* stre
     const size_t b_slots = up(cap * sizeof(uint64_t));
     const size_t b_nbr = up((size_t)m->ntiles * sc::kTileRows * sc::kTaps * sizeof(int32_t));
     const size_t b_mask = up((size_t)m->ntiles * sizeof(uint32_t));
-    m->block = dev_alloc(m, b_slots + b_nbr + b_mask + 256, s);
+    m->block = dev_alloc(m, b_slots + b_nbr + b_mask + up(sc::kStatusBlockBytes), s);
     if (!m->block) {
       delete m;
       fail(SC_ERR_ALLOC, "sc_build_map: device allocation failed (n=%lld)", (long long)n);
@@ -209,14 +209,15 @@ sc_handle sc_build_map(const int32_t* coords, int64_t n, int32_t res, void* stre
     m->nbr = reinterpret_cast<int32_t*>(base + b_slots);
     m->tile_mask = reinterpret_cast<uint32_t*>(base + b_slots + b_nbr);
     m->d_status = reinterpret_cast<uint32_t*>(base + b_slots + b_nbr + b_mask);
-    m->d_pairs = reinterpret_cast<unsigned long long*>(m->d_status + 2);
+    m->d_pairs = reinterpret_cast<unsigned long long*>(m->d_status + 4);
     cudaError_t e = sc::launch_map_init(m->hash, m->tile_mask, m->ntiles, m->d_status, s);
     if (e == cudaSuccess) e = sc::launch_hash_insert(coords, m->hash, m->d_status, s);
     if (e == cudaSuccess)
       e = sc::launch_neighbor_query(coords, m->hash, m->nbr, m->tile_mask, m->d_pairs,
                                     m->d_status, sc::kNbrTileMajor, s);
-    uint32_t host[4] = {0, 0, 0, 0};
-    if (e == cudaSuccess) e = cudaMemcpyAsync(host, m->d_status, 16, cudaMemcpyDeviceToHost, s);
+    uint32_t host[sc::kStatusBlockBytes / 4] = {};
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(host, m->d_status, sizeof(host), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) {
       release_buffers(m, s);
@@ -243,7 +244,12 @@ sc_handle sc_build_map(const int32_t* coords, int64_t n, int32_t res, void* stre
       return nullptr;
     }
     uint64_t pairs;
-    std::memcpy(&pairs, host + 2, sizeof(pairs));
+    pairs = 0;
+    for (int c = 0; c < sc::kPairCounters; ++c) {
+      uint64_t v;
+      std::memcpy(&v, host + 4 + 2 * c, sizeof(v));
+      pairs += v;
+    }
     m->npairs = (int64_t)pairs;
   }
   {

@@ -16,6 +16,14 @@ constexpr int kTaps = 27;
 constexpr int kCentre = 13;
 constexpr uint64_t kEmptySlot = ~0ull;
 
+// Status block of a map (16-byte aligned): four status words, then
+// kPairCounters 64-bit pair counters.  Each query block adds its pair count
+// to one counter (a counter per block-index residue, not one global counter:
+// tens of thousands of same-address atomics would serialise in one L2
+// slice); the host sums them.
+constexpr int kPairCounters = 32;
+constexpr int kStatusBlockBytes = 16 + 8 * kPairCounters;
+
 // Device status word bits (the map's `d_status`).
 enum : uint32_t {
   kStatRange = 1u,
@@ -330,7 +338,7 @@ struct sc_map {
   uint32_t* tile_mask;   // [ntiles] OR of the 27-bit presence masks of a tile's rows
   uint32_t* d_status;    // device status word + pair counter scratch
   void* block;           // the one device allocation the buffers above are carved from
-  unsigned long long* d_pairs;
+  unsigned long long* d_pairs;  // kPairCounters counters after the status words
   void* (*alloc)(size_t, void*, void*);
   void (*free_fn)(void*, void*, void*);
   void* alloc_ctx;
@@ -338,8 +346,8 @@ struct sc_map {
 
 namespace sc {
 
-// Clear a map's scratch: all slots empty, tile masks and the 16-byte status
-// block zero (slots 16-byte aligned).
+// Clear a map's scratch: all slots empty, tile masks and the status block
+// zero (slots 16-byte aligned).
 cudaError_t launch_map_init(const HashParams& hp, uint32_t* tile_mask, int64_t ntiles,
                             uint32_t* status, cudaStream_t s);
 cudaError_t launch_hash_insert(const int32_t* coords, const HashParams& hp, uint32_t* status,

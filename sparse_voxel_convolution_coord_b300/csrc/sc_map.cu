@@ -179,7 +179,9 @@ __global__ void __launch_bounds__(kTileRows) k_neighbor_query(
       cnt += s_cnt[w];
     }
     if (m) atomicOr(tile_mask + blockIdx.x, m);  // zeroed before the launch
-    if (cnt) atomicAdd(pair_count, (unsigned long long)cnt);
+    if (cnt)
+      atomicAdd(pair_count + (blockIdx.x * 9u + blockIdx.y) % kPairCounters,
+                (unsigned long long)cnt);
   }
 }
 
@@ -216,7 +218,7 @@ __global__ void __launch_bounds__(256) k_map_init(ulonglong2* __restrict__ slots
   const ulonglong2 ones = make_ulonglong2(kEmptySlot, kEmptySlot);
   for (int64_t i = t; i < npairs2; i += stride) slots[i] = ones;
   for (int64_t i = t; i < ntiles; i += stride) tile_mask[i] = 0u;
-  if (t < 4) status[t] = 0u;
+  if (t < kStatusBlockBytes / 4) status[t] = 0u;
 }
 
 cudaError_t launch_map_init(const HashParams& hp, uint32_t* tile_mask, int64_t ntiles,
@@ -224,6 +226,7 @@ cudaError_t launch_map_init(const HashParams& hp, uint32_t* tile_mask, int64_t n
   const int64_t npairs2 = (int64_t)(hp.cap_mask + 1) / 2;  // 16-byte stores
   const int64_t work = std::max<int64_t>(npairs2, ntiles);
   const int64_t blocks = std::min<int64_t>((work + 255) / 256, 148LL * 8);
+  static_assert(kStatusBlockBytes / 4 <= 256, "status block cleared by the first block");
   k_map_init<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, s>>>(
       reinterpret_cast<ulonglong2*>(hp.slots), npairs2, tile_mask, ntiles, status);
   return cudaGetLastError();

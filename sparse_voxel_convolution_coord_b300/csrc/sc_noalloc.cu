@@ -24,7 +24,7 @@ constexpr int64_t kNoAllocMaxTiles = kNoAllocMaxVoxels / sc::kTileRows;  // 4,09
 // Layout in 64-bit words: [slots | tile masks (2 per word) | status, pairs].
 constexpr uint64_t kMaskWordOffset = kNoAllocSlots;
 constexpr uint64_t kStatusWordOffset = kMaskWordOffset + kNoAllocMaxTiles / 2;
-constexpr uint64_t kScratchWords = kStatusWordOffset + 2;
+constexpr uint64_t kScratchWords = kStatusWordOffset + sc::kStatusBlockBytes / 8;
 
 static __device__ __align__(256) uint64_t g_noalloc_scratch[kScratchWords];
 
@@ -106,7 +106,7 @@ extern "C" SC_API sc_status sc_build_neighbor_table_noalloc(const int32_t* coord
   hp.n = n;
   uint32_t* tile_mask = reinterpret_cast<uint32_t*>(scratch + kMaskWordOffset);
   uint32_t* status = reinterpret_cast<uint32_t*>(scratch + kStatusWordOffset);
-  unsigned long long* pair_count = reinterpret_cast<unsigned long long*>(status + 2);
+  unsigned long long* pair_count = reinterpret_cast<unsigned long long*>(status + 4);
 
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The scratch keeps the previous call's contents: clear the slots in use and
@@ -117,8 +117,8 @@ extern "C" SC_API sc_status sc_build_neighbor_table_noalloc(const int32_t* coord
   if (e == cudaSuccess)
     e = sc::launch_neighbor_query(coords, hp, nbr_out, tile_mask, pair_count, status,
                                   sc::kNbrRowMajor, s);
-  uint32_t host[4] = {0, 0, 0, 0};
-  if (e == cudaSuccess) e = cudaMemcpyAsync(host, status, 16, cudaMemcpyDeviceToHost, s);
+  uint32_t host[sc::kStatusBlockBytes / 4] = {};
+  if (e == cudaSuccess) e = cudaMemcpyAsync(host, status, sizeof(host), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess)
     return report(SC_ERR_CUDA, "sc_build_neighbor_table_noalloc: CUDA error %lld", (long long)e);
@@ -137,7 +137,12 @@ extern "C" SC_API sc_status sc_build_neighbor_table_noalloc(const int32_t* coord
   if (st) return report(SC_ERR_TABLE_FULL, "sc_build_neighbor_table_noalloc: probe bound exceeded");
   if (pairs_out) {
     unsigned long long pc;
-    memcpy(&pc, host + 2, sizeof(pc));
+    pc = 0;
+    for (int c = 0; c < sc::kPairCounters; ++c) {
+      unsigned long long v;
+      memcpy(&v, host + 4 + 2 * c, sizeof(v));
+      pc += v;
+    }
     *pairs_out = (int64_t)pc;
   }
   return sc::set_last_error(SC_OK, "");
