@@ -71,6 +71,11 @@ constexpr int kTcThreads = 32 * (kMmaWarp + 1);
 
 constexpr int kSmemLimit = 227 * 1024;                  // opt-in dynamic shared memory per CTA
 constexpr int kNbrBytes = kTileRows * kTaps * 4;        // one tile's neighbour block, 13,824 B
+// Epilogue staging: each epilogue warp transposes its 32 rows x 32 columns
+// through shared memory (row stride 36 floats: 16-byte aligned, and both the
+// row-wise writes and the column-group reads are bank-conflict-free).
+constexpr int kStageRow = 36;
+constexpr int kEpiBytes = 4 * 32 * kStageRow * 4;       // 18,432 B
 constexpr uint64_t kWaitNs = 2000000000ull;             // bounded waits: 2 s
 constexpr uint64_t kDrainNs = 50000000ull;              // final drain after an abort: 50 ms
 
@@ -90,7 +95,13 @@ struct TcCfg {
   static constexpr int kBBytes = 64 * NPAD * 2;         // 64 K rows x NPAD bf16
   static constexpr int kBBoxes = kSegs * kBlocksN;      // TMA boxes of B per stage
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kFixed = 2 * kNbrBytes + NPAD * 4 + 256;  // nbr x2, bias, barriers
+  // Neighbour blocks: two (the next unit's prefetched during this one) for
+  // cout <= 64, whose short units would expose the refill; one otherwise,
+  // refilled after a unit's stages while the MMA drains the ring.
+  static constexpr int kNbrBufs = NPAD <= 64 ? 2 : 1;
+  // Fixed: neighbour block(s), the epilogue's staging (4 warps x 32 rows x
+  // kStageRow floats), bias, barriers.
+  static constexpr int kFixed = kNbrBufs * kNbrBytes + kEpiBytes + NPAD * 4 + 256;
   static constexpr int kStages0 = (kSmemLimit - 1024 - kFixed) / kStageBytes;
   static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kFixed;
@@ -188,8 +199,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + C::kStages * C::kABytes;
-  int32_t* s_nbr = reinterpret_cast<int32_t*>(sB + C::kStages * C::kBBytes);  // [2][27][128]
-  float* s_bias = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s_nbr) + 2 * kNbrBytes);
+  int32_t* s_nbr = reinterpret_cast<int32_t*>(sB + C::kStages * C::kBBytes);  // [bufs][27][128]
+  float* s_epi =
+      reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s_nbr) + C::kNbrBufs * kNbrBytes);
+  float* s_bias = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s_epi) + kEpiBytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(s_bias + NPAD);
   uint64_t* empty = full + C::kStages;
   uint64_t* acc_full = empty + C::kStages;
@@ -234,8 +247,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == kLoaderWarp) {
     // ------------------------------------------------------------ loader
-    // Lane 0: the neighbour block of each unit's tile (bulk copy, one unit
-    // ahead) and, per stage, this CTA's W boxes by tiled TMA.
+    // Lane 0: per stage, this CTA's W boxes by tiled TMA and, once the
+    // producers have released a neighbour-block buffer, the next unit's
+    // block (one bulk copy).
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, fills = 0;
       int buf = 0;
@@ -259,9 +273,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int64_t unit = cid; unit < nunits && ok; unit += ncl) {
         const uint32_t mask = unit_mask<CL>(p.tile_mask, unit, p.ntiles);
         const int nst = unit_stages<CS>(mask, p.cin);
-        if (!issue_nbr(unit + ncl, buf ^ 1)) {
-          ok = false;
-          break;
+        if constexpr (C::kNbrBufs == 2) {
+          if (!issue_nbr(unit + ncl, buf ^ 1)) {
+            ok = false;
+            break;
+          }
         }
         OffsetIter<CS> it(mask, p.cin);
         for (int s = 0; s < nst; ++s) {
@@ -296,7 +312,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             phase ^= 1u;
           }
         }
-        buf ^= 1;
+        // One buffer: the next unit's block as soon as every producer is
+        // done with this one (the MMA still holds up to kStages stages).
+        if constexpr (C::kNbrBufs == 1) {
+          if (ok && !issue_nbr(unit + ncl, 0)) ok = false;
+        }
+        buf ^= C::kNbrBufs - 1;
       }
       if (!ok) {
         *s_abort = 1;
@@ -386,7 +407,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (!ok) break;
       if (has_rows) mbar_arrive(&nbr_empty[buf]);  // this thread is done with the block
-      buf ^= 1;
+      buf ^= C::kNbrBufs - 1;
     }
     if (!ok) {
       *s_abort = 1;
@@ -457,27 +478,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      const int64_t row = (unit * CL + rank) * kTileRows + warp * 32 + lane;
+      const int64_t wrow0 = (unit * CL + rank) * kTileRows + warp * 32;  // this warp's rows
       const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + acc * NPAD;
-      float* orow = p.out + row * p.cout;
+      float* stg = s_epi + warp * (32 * kStageRow);
       for (int ch = 0; ch < nchunks; ++ch) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + ch * 32, v);
         tmem_ld_wait();
-        if (row < p.n) {
+        // Row `lane` (+ bias) into the staging block, 16 bytes at a time ...
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int c = ch * 32 + 4 * q;
-            if (c < p.cout) {
-              float4 o;
-              o.x = __uint_as_float(v[4 * q + 0]) + s_bias[c + 0];
-              o.y = __uint_as_float(v[4 * q + 1]) + s_bias[c + 1];
-              o.z = __uint_as_float(v[4 * q + 2]) + s_bias[c + 2];
-              o.w = __uint_as_float(v[4 * q + 3]) + s_bias[c + 3];
-              __stcs(reinterpret_cast<float4*>(orow + c), o);
-            }
-          }
+        for (int q = 0; q < 8; ++q) {
+          const int c = ch * 32 + 4 * q;
+          float4 o;
+          o.x = __uint_as_float(v[4 * q + 0]) + s_bias[c + 0];
+          o.y = __uint_as_float(v[4 * q + 1]) + s_bias[c + 1];
+          o.z = __uint_as_float(v[4 * q + 2]) + s_bias[c + 2];
+          o.w = __uint_as_float(v[4 * q + 3]) + s_bias[c + 3];
+          *reinterpret_cast<float4*>(stg + lane * kStageRow + 4 * q) = o;
         }
+        __syncwarp();
+        // ... and out again by column groups: each store instruction writes
+        // four rows x 128 contiguous bytes.
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int r = 4 * q + (lane >> 3), g = lane & 7;
+          const int c = ch * 32 + 4 * g;
+          const int64_t row = wrow0 + r;
+          const float4 o = *reinterpret_cast<const float4*>(stg + r * kStageRow + 4 * g);
+          if (row < p.n && c < p.cout) __stcs(reinterpret_cast<float4*>(p.out + row * p.cout + c), o);
+        }
+        __syncwarp();
       }
       tc_fence_before();
       mbar_arrive(&acc_empty[acc]);
