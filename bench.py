@@ -220,7 +220,7 @@ def run_reference(args):
 # valid only for the kernel source it was measured on (sha1 of the file).
 MEASURED_TRAFFIC = {
     # workload name: (sha1 of sc_conv_tc.cu, bytes per launch)
-    "sq3x64_30k_c256_bf16": ("39de549d4fae4f08ea5a6e81687dc7a11949809b", 22143232 + 73216),
+    "sq3x64_30k_c256_bf16": ("c8c28ddf7612bae086a6403a1871462a4580be26", 22086400 + 83968),
 }
 
 
