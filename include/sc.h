@@ -97,8 +97,13 @@ SC_API sc_handle sc_build_map(const int32_t* coords, int64_t n, int32_t res, voi
  *   out[o][:] = bias[:] + sum_k feats[nbr[o][k]][:] @ W[k]   (k with nbr >= 0)
  * ("Porting TRELLIS.2 ...", section V: gather-GEMM over the neighbour table,
  * half-precision inputs, single-precision accumulation, bias fused into the
- * same pass).  Each output row is written exactly once, by the one tile that
- * owns it; no atomics.
+ * same pass).  On the SC_BF16 path each 128-row tile has one owner, except
+ * the tiles of a last, partial round over the SMs: their K range may be
+ * split over several CTAs that add into the (zeroed) rows with float atomics,
+ * so those rows' sums are taken in an order that can vary from run to run
+ * (differences at fp32 rounding level).  sc_set_deterministic(1) limits the
+ * split to two parts, whose sum is order-independent, making repeated calls
+ * bit-identical.
  *
  *   feats   device [n][cin], dtype `dtype`, row-major, 16-byte aligned.
  *   weight  device [27][cin][cout], dtype `dtype`, row-major, 16-byte aligned.
@@ -122,6 +127,23 @@ SC_API sc_status sc_forward(sc_handle h, const void* feats, const void* weight, 
  * sc_build_map) gives SC_ERR_BAD_HANDLE and is not touched.  NULL is a no-op.
  */
 SC_API sc_status sc_free_map(sc_handle h, void* stream);
+
+/*
+ * Deterministic mode for sc_forward (process-wide; default 0).  With 1, every
+ * call on the same inputs returns bit-identical outputs, at the cost of the
+ * tail split described under sc_forward (a last partial round of tiles then
+ * runs as fewer, longer parts).  Returns SC_OK, or SC_ERR_INVALID_ARG for a
+ * value other than 0 or 1.
+ */
+SC_API sc_status sc_set_deterministic(int32_t enable);
+
+/*
+ * Number of GPU kernels this library has launched in this process, counted on
+ * the host at each launch (map build: 3 per sc_build_map; sc_forward: 1, or 2
+ * when the bf16 path zeroes split rows first; 1 per sc_get_neighbor_table; 3
+ * or 4 per sc_get_pairs).  For measuring launches over a region of code.
+ */
+SC_API uint64_t sc_kernel_launches(void);
 
 /* Number of rows n of the map, or -1 (and SC_ERR_BAD_HANDLE) for a dead handle. */
 SC_API int64_t sc_map_size(sc_handle h);

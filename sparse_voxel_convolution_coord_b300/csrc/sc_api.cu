@@ -5,6 +5,7 @@
 // sc_conv_tc.cu and sc_conv_simt.cu; nothing here computes on the host.
 #include <cstdarg>
 #include <cstdio>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <unordered_set>
@@ -123,6 +124,14 @@ sc_status set_last_error(sc_status st, const char* msg) {
 }
 }  // namespace sc
 
+namespace sc {
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+void note_launches(int k) { g_launches.fetch_add((uint64_t)k, std::memory_order_relaxed); }
+uint64_t launches() { return g_launches.load(std::memory_order_relaxed); }
+}  // namespace sc
+
 extern "C" {
 
 sc_status sc_last_error(void) { return t_status; }
@@ -136,6 +145,15 @@ sc_status sc_set_allocator(void* (*alloc)(size_t, void*, void*),
   g_alloc.alloc = alloc;
   g_alloc.free_fn = free_fn;
   g_alloc.ctx = ctx;
+  return ok();
+}
+
+uint64_t sc_kernel_launches(void) { return sc::launches(); }
+
+sc_status sc_set_deterministic(int32_t enable) {
+  if (enable != 0 && enable != 1)
+    return fail(SC_ERR_INVALID_ARG, "sc_set_deterministic: enable must be 0 or 1");
+  sc::set_deterministic(enable != 0);
   return ok();
 }
 

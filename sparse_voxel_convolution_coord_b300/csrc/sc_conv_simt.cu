@@ -133,6 +133,7 @@ cudaError_t launch_simt(const sc_map* m, const float* feats, const float* w, con
   const unsigned blocks = (unsigned)((m->n + kSimtWarps - 1) / kSimtWarps);
   k_conv_simt_f32<J><<<blocks, kSimtWarps * 32, smem, s>>>(m->nbr, m->n, feats, w, bias, out, cin,
                                                            cout);
+  note_launches(1);
   return cudaGetLastError();
 }
 

@@ -10,12 +10,24 @@
 // How: an output-stationary implicit GEMM.  A CTA owns a tile of 128 output
 // rows; the GEMM's K dimension is (offset, input channel).  For each offset
 // present in the tile (its 27-bit OR mask), the 128 neighbour rows are
-// gathered straight from the feature matrix by TMA (tile::gather4, four rows
-// per instruction, absent neighbours given an out-of-range row so the copy
-// fills zeros) and W[k] arrives by tiled TMA; a single thread issues
+// gathered straight from the feature matrix by cp.async (absent neighbours
+// zero-filled) and W[k] arrives by tiled TMA; a single thread issues
 // tcgen05.mma (M = 128, N = cout padded to 64, K = 16, bf16 x bf16 -> fp32)
 // into a TMEM accumulator.  Each output row belongs to exactly one tile, so
 // the epilogue (TMEM -> registers, + bias, fp32 store) needs no atomics.
+//
+// Tail split: the grid is persistent (one cluster per pair of SMs), so when
+// the units do not divide evenly over the clusters the last, partial wave
+// would leave most SMs idle.  The host then splits each unit of that wave
+// into S parts by ranges of its K stages; parts are spread over all
+// clusters, and each adds its partial accumulator into the output (zeroed
+// beforehand) with 16-byte float atomics, the last part adding the bias.
+// Those rows' sums are then taken in an order that can vary between runs.
+// The parts run first, so that their atomic epilogues overlap other CTAs'
+// main loops and the kernel ends on plain stores.  The rows are zeroed by a
+// small kernel launched just before, with this one as its programmatic
+// dependent: both run at once, and only the epilogue waits for the zeroing
+// (griddepcontrol.wait) before its first atomic add.
 //
 // Clusters: with CL = 2 the two CTAs of a cluster work on adjacent tiles in
 // lock step (the union of their offset masks) and share each W slice: every
@@ -50,6 +62,7 @@
 //     128-byte swizzle; LBO = 8 KB between 64-column blocks, SBO = 1 KB
 //     between 8-row groups.
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -122,9 +135,38 @@ struct TcArgs {
   uint32_t* status;
   int64_t n;
   int64_t ntiles;
+  int64_t whole;   // units 0 .. whole-1 are one work item each
+  int64_t tail;    // units whole .. whole+tail-1 are `split` items each
+  int64_t nparts;  // tail * split
+  int64_t nitems;  // nparts + whole
+  int split;
   int cin;
   int cout;
 };
+
+// Work item i: part `part` of a tail unit (items 0 .. nparts-1, numbered
+// part-major, so a unit's parts go to different clusters and run
+// concurrently), then the whole units (part < 0).
+struct WorkItem {
+  int64_t unit;
+  int part;
+};
+__device__ __forceinline__ WorkItem work_item(const TcArgs& p, int64_t i) {
+  if (i >= p.nparts) return {i - p.nparts, -1};
+  return {p.whole + i % p.tail, (int)(i / p.tail)};
+}
+// Stage range [s0, s1) of an item of a unit with nst stages.  The last part
+// is never empty when nst > 0, so it is the one that adds the bias.
+__device__ __forceinline__ void item_range(const WorkItem& w, int split, int nst, int& s0,
+                                           int& s1) {
+  if (w.part < 0) {
+    s0 = 0;
+    s1 = nst;
+  } else {
+    s0 = (int)((int64_t)w.part * nst / split);
+    s1 = (int)((int64_t)(w.part + 1) * nst / split);
+  }
+}
 
 // Bounded wait with its own limit; ignores the abort flag (used to drain).
 __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
@@ -170,6 +212,18 @@ struct OffsetIter {
   uint32_t rem;
   int cblk = 0, cblocks;
   __device__ __forceinline__ OffsetIter(uint32_t mask, int cin) : rem(mask), cblocks(cin >> 6) {}
+  // Step over the first `n` stages.
+  __device__ __forceinline__ void skip(int n) {
+    if constexpr (CS == 64) {
+      cblk += n;
+      while (cblk >= cblocks) {
+        cblk -= cblocks;
+        rem &= rem - 1u;
+      }
+    } else {
+      for (int i = 0; i < n * (64 / CS); ++i) rem &= rem - 1u;
+    }
+  }
   __device__ __forceinline__ int next(int (&ks)[64 / CS]) {
     if constexpr (CS == 64) {
       ks[0] = __ffs(rem) - 1;
@@ -189,6 +243,16 @@ struct OffsetIter {
     }
   }
 };
+
+// Zeroes the rows the split units add into.  It lets its dependent (the
+// convolution) launch at once; the dependent waits for this grid's
+// completion only where it reads these rows.
+__global__ void __launch_bounds__(256) k_zero_rows(float4* __restrict__ p, int64_t n4) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride)
+    p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
 
 template <int NPAD, int CS, int CL>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -217,7 +281,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
   const int64_t cid = blockIdx.x / CL;
   const int64_t ncl = gridDim.x / CL;
-  const int64_t nunits = (p.ntiles + CL - 1) / CL;
   constexpr uint16_t kAllCtas = (uint16_t)((1u << CL) - 1u);
 
   if (threadIdx.x == 0) {
@@ -254,10 +317,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t stage = 0, phase = 0, fills = 0;
       int buf = 0;
       bool ok = true;
-      // Refill buffer b once every A producer has released its contents.
-      auto issue_nbr = [&](int64_t unit, int b) -> bool {
-        const int64_t t = unit * CL + rank;
-        if (unit >= nunits || t >= p.ntiles) return true;
+      // Refill buffer b with item i's block once every A producer has
+      // released its contents.
+      auto issue_nbr = [&](int64_t i, int b) -> bool {
+        if (i >= p.nitems) return true;
+        const int64_t t = work_item(p, i).unit * CL + rank;
+        if (t >= p.ntiles) return true;
         if ((fills >> (2 + b)) & 1u) {  // used before: wait for the release
           if (!mbar_wait_bounded(&nbr_empty[b], ((fills >> b) & 1u) ^ 1u, abort_flag))
             return false;
@@ -270,17 +335,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return true;
       };
       ok = issue_nbr(cid, 0);
-      for (int64_t unit = cid; unit < nunits && ok; unit += ncl) {
-        const uint32_t mask = unit_mask<CL>(p.tile_mask, unit, p.ntiles);
-        const int nst = unit_stages<CS>(mask, p.cin);
+      for (int64_t item = cid; item < p.nitems && ok; item += ncl) {
+        const WorkItem wi = work_item(p, item);
+        const uint32_t mask = unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles);
+        int s0, s1;
+        item_range(wi, p.split, unit_stages<CS>(mask, p.cin), s0, s1);
         if constexpr (C::kNbrBufs == 2) {
-          if (!issue_nbr(unit + ncl, buf ^ 1)) {
+          if (!issue_nbr(item + ncl, buf ^ 1)) {
             ok = false;
             break;
           }
         }
         OffsetIter<CS> it(mask, p.cin);
-        for (int s = 0; s < nst; ++s) {
+        it.skip(s0);
+        for (int s = s0; s < s1; ++s) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -315,7 +383,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // One buffer: the next unit's block as soon as every producer is
         // done with this one (the MMA still holds up to kStages stages).
         if constexpr (C::kNbrBufs == 1) {
-          if (ok && !issue_nbr(unit + ncl, 0)) ok = false;
+          if (ok && !issue_nbr(item + ncl, 0)) ok = false;
         }
         buf ^= C::kNbrBufs - 1;
       }
@@ -346,11 +414,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t stage = 0, phase = 0, nbr_phase = 0;
     int buf = 0;
     bool ok = true;
-    for (int64_t unit = cid; unit < nunits && ok; unit += ncl) {
-      const int64_t tile = unit * CL + rank;
+    for (int64_t item = cid; item < p.nitems && ok; item += ncl) {
+      const WorkItem wi = work_item(p, item);
+      const int64_t tile = wi.unit * CL + rank;
       const bool has_rows = tile < p.ntiles;
-      const uint32_t mask = unit_mask<CL>(p.tile_mask, unit, p.ntiles);
-      const int nst = unit_stages<CS>(mask, p.cin);
+      const uint32_t mask = unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles);
+      int s0, s1;
+      item_range(wi, p.split, unit_stages<CS>(mask, p.cin), s0, s1);
       if (has_rows) {
         if (!mbar_wait_bounded(&nbr_full[buf], (nbr_phase >> buf) & 1u, abort_flag)) {
           ok = false;
@@ -360,7 +430,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       const int32_t* nb = s_nbr + buf * (kTileRows * kTaps);
       OffsetIter<CS> it(mask, p.cin);
-      for (int s = 0; s < nst; ++s) {
+      it.skip(s0);
+      for (int s = s0; s < s1; ++s) {
         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -420,8 +491,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int64_t unit = cid; unit < nunits && ok; unit += ncl) {
-        const int nst = unit_stages<CS>(unit_mask<CL>(p.tile_mask, unit, p.ntiles), p.cin);
+      for (int64_t item = cid; item < p.nitems && ok; item += ncl) {
+        const WorkItem wi = work_item(p, item);
+        int s0, s1;
+        item_range(wi, p.split, unit_stages<CS>(unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles), p.cin),
+                   s0, s1);
+        if (s0 == s1) continue;  // an empty part: no accumulator, no epilogue
+        const int nst = s1 - s0;
         if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -471,14 +547,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ------------------------------------------------------------ epilogue
     uint32_t acc = 0, acc_phase = 0;
     bool ok = true;
+    bool rows_zeroed = false;  // the zeroing grid is complete and visible
     const int nchunks = (p.cout + 31) >> 5;
-    for (int64_t unit = cid; unit < nunits && ok; unit += ncl) {
+    for (int64_t item = cid; item < p.nitems && ok; item += ncl) {
+      const WorkItem wi = work_item(p, item);
+      if (wi.part >= 0) {  // a whole unit has rows, so its centre offset: never empty
+        int s0, s1;
+        item_range(wi, p.split,
+                   unit_stages<CS>(unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles), p.cin), s0, s1);
+        if (s0 == s1) continue;
+      }
+      // Whole units store; parts add into the zeroed rows, the last with the bias.
+      const bool add = wi.part >= 0;
+      const float bscale = (wi.part < p.split - 1) && add ? 0.f : 1.f;
+      if (add && !rows_zeroed) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        rows_zeroed = true;
+      }
       if (!mbar_wait_bounded(&acc_full[acc], acc_phase, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int64_t wrow0 = (unit * CL + rank) * kTileRows + warp * 32;  // this warp's rows
+      const int64_t wrow0 = (wi.unit * CL + rank) * kTileRows + warp * 32;  // this warp's rows
       const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + acc * NPAD;
       float* stg = s_epi + warp * (32 * kStageRow);
       for (int ch = 0; ch < nchunks; ++ch) {
@@ -490,10 +581,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int q = 0; q < 8; ++q) {
           const int c = ch * 32 + 4 * q;
           float4 o;
-          o.x = __uint_as_float(v[4 * q + 0]) + s_bias[c + 0];
-          o.y = __uint_as_float(v[4 * q + 1]) + s_bias[c + 1];
-          o.z = __uint_as_float(v[4 * q + 2]) + s_bias[c + 2];
-          o.w = __uint_as_float(v[4 * q + 3]) + s_bias[c + 3];
+          o.x = __uint_as_float(v[4 * q + 0]) + bscale * s_bias[c + 0];
+          o.y = __uint_as_float(v[4 * q + 1]) + bscale * s_bias[c + 1];
+          o.z = __uint_as_float(v[4 * q + 2]) + bscale * s_bias[c + 2];
+          o.w = __uint_as_float(v[4 * q + 3]) + bscale * s_bias[c + 3];
           *reinterpret_cast<float4*>(stg + lane * kStageRow + 4 * q) = o;
         }
         __syncwarp();
@@ -505,7 +596,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int c = ch * 32 + 4 * g;
           const int64_t row = wrow0 + r;
           const float4 o = *reinterpret_cast<const float4*>(stg + r * kStageRow + 4 * g);
-          if (row < p.n && c < p.cout) __stcs(reinterpret_cast<float4*>(p.out + row * p.cout + c), o);
+          if (row < p.n && c < p.cout) {
+            float4* dst = reinterpret_cast<float4*>(p.out + row * p.cout + c);
+            if (add)
+              atomicAdd(dst, o);
+            else
+              __stcs(dst, o);
+          }
         }
         __syncwarp();
       }
@@ -584,6 +681,39 @@ int cluster_size(int npad) {
   return npad > 64 ? 2 : 1;
 }
 
+// Parts per unit of the last, partial round of units (1 = no split).  With
+// G clusters, `waves` full rounds and `rem` units left over, the leftover
+// round takes ceil(rem * S / G) / S of a unit's time when each of its units
+// is split S ways.  A split costs a zeroing pass and atomic adds (charged as
+// 0.05 + 0.04 S of a unit), each part should keep at least six K stages, and
+// a predicted gain under 5% is not taken (a split of 563 units over 74
+// clusters, predicted 2%, measured 1% slower).
+std::atomic<bool> g_deterministic{false};
+
+int tail_split(int64_t nunits, int64_t G, int max_stages) {
+  static const int forced = [] {
+    const char* e = std::getenv("SC_CONV_SPLIT");
+    return e ? std::atoi(e) : 0;
+  }();
+  const int64_t rem = nunits >= G ? nunits % G : nunits;
+  if (rem == 0 || G <= 0) return 1;
+  // Two addends into a zeroed row sum the same in either order; three do not.
+  const int cap = std::max(1, std::min(g_deterministic.load() ? 2 : 8, max_stages / 6));
+  if (forced > 0) return std::min(forced, cap);
+  const double waves = (double)(nunits / G);
+  const double t1 = waves + 1.0;
+  int best = 1;
+  double best_t = t1;
+  for (int S = 2; S <= cap; ++S) {
+    const double t = waves + (double)((rem * S + G - 1) / G) / S + 0.05 + 0.04 * S;
+    if (t < best_t - 1e-9) {
+      best_t = t;
+      best = S;
+    }
+  }
+  return best_t < 0.95 * t1 ? best : 1;
+}
+
 template <int NPAD, int CS, int CL>
 cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, const float* bias,
                          float* out, int cin, int cout, cudaStream_t s) {
@@ -595,11 +725,13 @@ cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, cons
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
 
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.blockDim = dim3(kTcThreads, 1, 1);
@@ -643,9 +775,30 @@ cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, cons
   a.cin = cin;
   a.cout = cout;
   const int64_t nunits = (m->ntiles + CL - 1) / CL;
-  cfg.gridDim = dim3((unsigned)(CL * std::min<int64_t>(nunits, max_clusters)), 1, 1);
+  if (nunits == 0) return cudaSuccess;
+  const int max_stages = CS == 64 ? kTaps * (cin / 64) : (kTaps + 64 / CS - 1) / (64 / CS);
+  const int split = tail_split(nunits, max_clusters, max_stages);
+  a.split = split;
+  a.tail = split > 1 ? (nunits >= max_clusters ? nunits % max_clusters : nunits) : 0;
+  a.whole = nunits - a.tail;
+  a.nparts = a.tail * split;
+  a.nitems = a.nparts + a.whole;
+  if (a.tail > 0) {
+    // The split units' rows start at zero; their parts add into them.  The
+    // convolution is this launch's programmatic dependent (attribute 1).
+    const int64_t row0 = a.whole * CL * kTileRows;
+    const int64_t n4 = (m->n - row0) * cout / 4;  // cout is a multiple of 16
+    const int64_t zb = std::min<int64_t>((n4 + 255) / 256, 2 * 148);
+    k_zero_rows<<<(unsigned)zb, 256, 0, s>>>(reinterpret_cast<float4*>(out + row0 * cout), n4);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    note_launches(1);
+    cfg.numAttrs = 2;
+  }
+  cfg.gridDim = dim3((unsigned)(CL * std::min<int64_t>(a.nitems, max_clusters)), 1, 1);
   void* args[2] = {&tm_b, &a};
   e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kern), args);
+  if (e == cudaSuccess) note_launches(1);
   return e;
 }
 
@@ -666,6 +819,8 @@ cudaError_t launch_npad(const sc_map* m, const void* feats, const void* w, const
 }
 
 }  // namespace
+
+void set_deterministic(bool on) { g_deterministic.store(on); }
 
 bool conv_tc_supported(int cin, int cout) {
   const bool cin_ok = cin == 16 || cin == 32 || (cin % 64 == 0 && cin >= 64 && cin <= 1024);

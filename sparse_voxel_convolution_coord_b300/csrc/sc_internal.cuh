@@ -368,6 +368,12 @@ cudaError_t launch_conv_tc_bf16(const sc_map* m, const void* feats, const void* 
                                 const float* bias, float* out, int cin, int cout,
                                 cudaStream_t s);
 bool conv_tc_supported(int cin, int cout);
+// Process-wide count of the kernels this library has launched (host side).
+void note_launches(int k);
+uint64_t launches();
+// Deterministic mode: the tensor-core kernel splits a unit in at most two
+// parts (a + b == b + a in fp32), so repeated calls are bit-identical.
+void set_deterministic(bool on);
 // Record a failure (or SC_OK with an empty message) as the calling thread's
 // last error; returns st.
 sc_status set_last_error(sc_status st, const char* msg);

@@ -229,6 +229,7 @@ cudaError_t launch_map_init(const HashParams& hp, uint32_t* tile_mask, int64_t n
   static_assert(kStatusBlockBytes / 4 <= 256, "status block cleared by the first block");
   k_map_init<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, s>>>(
       reinterpret_cast<ulonglong2*>(hp.slots), npairs2, tile_mask, ntiles, status);
+  note_launches(1);
   return cudaGetLastError();
 }
 
@@ -238,6 +239,7 @@ cudaError_t launch_hash_insert(const int32_t* coords, const HashParams& hp, uint
   const int64_t blocks = (hp.n + kInsertThreads - 1) / kInsertThreads;
   k_hash_insert<<<(unsigned)blocks, kInsertThreads, 0, s>>>(reinterpret_cast<const int4*>(coords),
                                                             hp, status);
+  note_launches(1);
   return cudaGetLastError();
 }
 
@@ -253,12 +255,14 @@ cudaError_t launch_neighbor_query(const int32_t* coords, const HashParams& hp, i
     k_neighbor_query<kNbrTileMajor><<<grid, kTileRows, 0, s>>>(c4, hp, nbr, tile_mask, pair_count);
   else
     k_neighbor_query<kNbrRowMajor><<<grid, kTileRows, 0, s>>>(c4, hp, nbr, tile_mask, pair_count);
+  note_launches(1);
   return cudaGetLastError();
 }
 
 cudaError_t launch_nbr_to_row_major(const sc_map* m, int32_t* nbr_out, cudaStream_t s) {
   if (m->n == 0) return cudaSuccess;
   k_nbr_to_row_major<<<(unsigned)m->ntiles, kTileRows, 0, s>>>(m->nbr, m->n, nbr_out);
+  note_launches(1);
   return cudaGetLastError();
 }
 
@@ -362,6 +366,7 @@ cudaError_t launch_pairs(const sc_map* m, int64_t* off_host, int32_t* in, int32_
   if (in || out)
     k_pairs_write<<<(unsigned)nblocks, kTileRows, 0, s>>>(m->nbr, nblocks, counts, in, out);
   k_pairs_offsets<<<1, 32, 0, s>>>(counts, nblocks, total, off28);
+  note_launches((in || out) ? 4 : 3);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaMemcpyAsync(off_host, off28, 28 * sizeof(int64_t), cudaMemcpyDeviceToHost, s);

@@ -25,6 +25,16 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, name), name
 
 
+def test_deterministic_switch_checks_its_argument(lib):
+    assert lib.sc_set_deterministic(2) == sc.SC_ERR_INVALID_ARG
+    assert lib.sc_set_deterministic(1) == sc.SC_OK
+    assert lib.sc_set_deterministic(0) == sc.SC_OK
+
+
+def test_launch_counter_is_exported(lib):
+    assert sc.sc_kernel_launches() >= 0
+
+
 def test_version(lib):
     assert "sm_103a" in sc.sc_version()
 
