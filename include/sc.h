@@ -85,9 +85,12 @@ typedef enum { SC_F32 = 0, SC_BF16 = 1 } sc_dtype;
  * (max batch + 1) * res^3 must be <= 2^(64 - bitlen(n)); e.g. res = 1024
  * with n < 2^24 allows 512 batch elements), SC_ERR_INVALID_ARG,
  * SC_ERR_ALLOC or SC_ERR_CUDA.
- * The call synchronises `stream` exactly once, to read the device status
- * word and the pair count; when it returns, every buffer of the map is ready
- * for use on any stream.  The handle owns its device memory (hash table,
+ * Keys are 32-bit whenever batch * res^3 stays below 2^32 - 1 (at res = 64,
+ * batch indices below 16,383); a batch index beyond that makes the build
+ * run a second time with 64-bit keys.
+ * The call synchronises `stream` once (twice in that retry), to read the
+ * device status word and the pair count; when it returns, every buffer of
+ * the map is ready for use on any stream.  The handle owns its device memory (hash table,
  * neighbour table nbr[n][27], per-tile offset masks) until sc_free_map.
  */
 SC_API sc_handle sc_build_map(const int32_t* coords, int64_t n, int32_t res, void* stream);

@@ -129,6 +129,27 @@ namespace {
 std::atomic<uint64_t> g_launches{0};
 }
 void note_launches(int k) { g_launches.fetch_add((uint64_t)k, std::memory_order_relaxed); }
+
+// Pinned host block for a build's status read-back, one per host thread
+// (a copy into pageable memory goes through a driver staging buffer).
+// nullptr if pinned memory cannot be had; callers then use their own.
+uint32_t* status_readback_buffer() {
+  struct Block {
+    uint32_t* p = nullptr;
+    ~Block() {
+      if (p) cudaFreeHost(p);
+    }
+  };
+  thread_local Block b;
+  if (!b.p) {
+    void* q = nullptr;
+    if (cudaHostAlloc(&q, kStatusBlockBytes, cudaHostAllocPortable) == cudaSuccess)
+      b.p = static_cast<uint32_t*>(q);
+    else
+      cudaGetLastError();
+  }
+  return b.p;
+}
 uint64_t launches() { return g_launches.load(std::memory_order_relaxed); }
 }  // namespace sc
 
@@ -183,30 +204,14 @@ sc_handle sc_build_map(const int32_t* coords, int64_t n, int32_t res, void* stre
   m->ntiles = (n + sc::kTileRows - 1) / sc::kTileRows;
 
   if (n > 0) {
-    const int vbits = bit_length((uint64_t)n);
-    const int kbits = 64 - vbits;
-    const uint64_t res3 = (uint64_t)res * res * res;
-    const uint64_t kspace = (kbits >= 64) ? ~0ull : (1ull << kbits);
-    const uint64_t bmax = kspace / res3;
-    if (bmax == 0) {
+    const int log2cap = sc::hash_log2cap(n);
+    const uint64_t cap = 1ull << log2cap;
+    if (!sc::make_hash_params(m->hash, nullptr, n, res, log2cap, true)) {
       delete m;
-      fail(SC_ERR_UNSUPPORTED, "sc_build_map: res^3 exceeds the 2^%d key space for n=%lld", kbits,
-           (long long)n);
+      fail(SC_ERR_UNSUPPORTED, "sc_build_map: res^3 exceeds the 2^%d key space for n=%lld",
+           64 - bit_length((uint64_t)n), (long long)n);
       return nullptr;
     }
-    uint64_t cap = 64;
-    int log2cap = 6;
-    while (cap < 2ull * (uint64_t)n) {
-      cap <<= 1;
-      ++log2cap;
-    }
-    m->hash.cap_mask = cap - 1;
-    m->hash.log2cap = log2cap;
-    m->hash.vbits = vbits;
-    m->hash.res = res;
-    m->hash.bres = (res + 1) / 2;
-    m->hash.bmax = bmax;
-    m->hash.n = n;
     // One allocation, carved (every piece 256-byte aligned): the hash table,
     // the tile-major neighbour table [ntiles][27][128] (pad rows -1: a
     // tile's rows are contiguous per offset, and a tile's whole 13,824-byte
@@ -228,21 +233,35 @@ sc_handle sc_build_map(const int32_t* coords, int64_t n, int32_t res, void* stre
     m->tile_mask = reinterpret_cast<uint32_t*>(base + b_slots + b_nbr);
     m->d_status = reinterpret_cast<uint32_t*>(base + b_slots + b_nbr + b_mask);
     m->d_pairs = reinterpret_cast<unsigned long long*>(m->d_status + 4);
-    cudaError_t e = sc::launch_map_init(m->hash, m->tile_mask, m->ntiles, m->d_status, s);
-    if (e == cudaSuccess) e = sc::launch_hash_insert(coords, m->hash, m->d_status, s);
-    if (e == cudaSuccess)
-      e = sc::launch_neighbor_query(coords, m->hash, m->nbr, m->tile_mask, m->d_pairs,
-                                    m->d_status, sc::kNbrTileMajor, s);
-    uint32_t host[sc::kStatusBlockBytes / 4] = {};
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(host, m->d_status, sizeof(host), cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    // The three kernels, then one synchronisation for the status and the
+    // pair count.  A batch index beyond the 32-bit key space (rare: more
+    // than (2^32 - 1) / res^3 batch elements) is retried once with 64-bit
+    // keys in the same buffers.
+    uint32_t host_local[sc::kStatusBlockBytes / 4] = {};
+    uint32_t* host = sc::status_readback_buffer();
+    if (!host) host = host_local;
+    cudaError_t e = cudaSuccess;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+      e = sc::launch_map_init(m->hash, m->tile_mask, m->ntiles, m->d_status, s);
+      if (e == cudaSuccess) e = sc::launch_hash_insert(coords, m->hash, m->d_status, s);
+      if (e == cudaSuccess)
+        e = sc::launch_neighbor_query(coords, m->hash, m->nbr, m->tile_mask, m->d_pairs,
+                                      m->d_status, sc::kNbrTileMajor, s);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(host, m->d_status, sc::kStatusBlockBytes, cudaMemcpyDeviceToHost, s);
+      if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+      if (e != cudaSuccess || !m->hash.k32 || !(host[0] & sc::kStatKeySpace) ||
+          (host[0] & sc::kStatRange))
+        break;
+      if (!sc::make_hash_params(m->hash, m->hash.slots, n, res, log2cap, false)) break;
+    }
     if (e != cudaSuccess) {
       release_buffers(m, s);
       delete m;
       fail_cuda(e, "sc_build_map");
       return nullptr;
     }
+    const uint64_t bmax = m->hash.bmax;
     const uint32_t st = host[0];
     if (st) {
       release_buffers(m, s);

@@ -34,9 +34,17 @@ enum : uint32_t {
 };
 
 // ---------------------------------------------------------------------------
-// Coordinate hash: packed 64-bit slots (key << vbits | row), empty = all ones.
-// key = ((b * res + x) * res + y) * res + z; vbits = bit length of n, so a
-// row index never fills its field and a live slot is never all ones.
+// Coordinate hash: packed 64-bit slots, empty = all ones, over the key
+// key = ((b * res + x) * res + y) * res + z.  Two packings:
+//   32-bit keys (k32, whenever batch x res^3 fits below 2^32 - 1 and the
+//     table has at most 2^32 slots): slot = key << 32 | flag << 31 | row.
+//     The flag of a slot is set when a key whose home it is had to move on
+//     (its home was taken), so a lookup that finds another key at its home
+//     slot with the flag clear knows at once that its key is absent.  All
+//     hashing is 32-bit arithmetic.
+//   64-bit keys otherwise: slot = key << vbits | row, vbits = bit length of
+//     n, so a row index never fills its field and a live slot is never all
+//     ones; lookups probe until their key or an empty slot.
 //
 // Home slots preserve locality: the grid is cut into 2x2x2 bricks, a brick
 // hashes to a group of 8 consecutive slots (64 bytes) and a voxel's home is
@@ -52,7 +60,8 @@ struct HashParams {
   uint64_t* slots;
   uint64_t cap_mask;   // capacity - 1 (capacity a power of two, >= 64)
   int log2cap;
-  int vbits;
+  int k32;             // 32-bit keys (see above)
+  int vbits;           // 64-bit keys: bits of the row field
   int res;
   int bres;            // bricks per axis: (res + 1) / 2
   uint64_t bmax;       // batch indices must be < bmax
@@ -76,6 +85,58 @@ __device__ __forceinline__ uint64_t home_slot(const HashParams& hp, int b, int x
 // Odd probe stride of a key (a second multiplicative hash).
 __device__ __forceinline__ uint64_t probe_step(const HashParams& hp, uint64_t key) {
   return ((key * 0xC2B2AE3D27D4EB4Full) >> (64 - hp.log2cap)) | 1ull;
+}
+
+// The same three functions with 32-bit keys (32-bit multiplicative hashes).
+__device__ __forceinline__ uint32_t cell_key32(const HashParams& hp, int b, int x, int y, int z) {
+  const uint32_t r = (uint32_t)hp.res;
+  return (((uint32_t)b * r + (uint32_t)x) * r + (uint32_t)y) * r + (uint32_t)z;
+}
+__device__ __forceinline__ uint32_t group32(const HashParams& hp, uint32_t brick) {
+  return (brick * 0x9E3779B9u) >> (32 - (hp.log2cap - 3));
+}
+__device__ __forceinline__ uint32_t home_slot32(const HashParams& hp, int b, int x, int y, int z) {
+  const uint32_t br = (uint32_t)hp.bres;
+  const uint32_t brick =
+      (((uint32_t)b * br + (uint32_t)(x >> 1)) * br + (uint32_t)(y >> 1)) * br + (uint32_t)(z >> 1);
+  return (group32(hp, brick) << 3) | (uint32_t)(((x & 1) << 2) | ((y & 1) << 1) | (z & 1));
+}
+__device__ __forceinline__ uint32_t probe_step32(const HashParams& hp, uint32_t key) {
+  return ((key * 0xC2B2AE35u) >> (32 - hp.log2cap)) | 1u;
+}
+constexpr uint64_t kMovedFlag = 1ull << 31;  // 32-bit keys: a key homed here moved on
+constexpr uint32_t kRowMask32 = 0x7fffffffu;
+
+// Host: hash parameters for n >= 1 rows at resolution res in 2^log2cap slots
+// (6 <= log2cap), with 32-bit keys when they fit (and k32_allowed).  Returns
+// false when not even batch 0 fits the key.
+inline bool make_hash_params(HashParams& hp, uint64_t* slots, int64_t n, int res, int log2cap,
+                             bool k32_allowed) {
+  const uint64_t res3 = (uint64_t)res * res * res;
+  const int vbits = 64 - __builtin_clzll((unsigned long long)n);
+  hp.slots = slots;
+  hp.cap_mask = (1ull << log2cap) - 1ull;
+  hp.log2cap = log2cap;
+  hp.vbits = vbits;
+  hp.res = res;
+  hp.bres = (res + 1) / 2;
+  hp.n = n;
+  hp.k32 = k32_allowed && log2cap <= 32 && res3 <= 0xffffffffull;
+  if (hp.k32) {
+    hp.bmax = 0xffffffffull / res3;  // keys <= 2^32 - 2: a live slot is never all ones
+    return true;
+  }
+  hp.bmax = (1ull << (64 - vbits)) / res3;
+  return hp.bmax > 0;
+}
+
+// Host: log2 of the table capacity for n rows, load factor <= 1/4 (a
+// brick's cells share a group of 8 slots; at load 1/2 a third of the
+// lookups of absent neighbours met another key at home).
+inline int hash_log2cap(int64_t n) {
+  int l = 6;
+  while ((1ull << l) < 4ull * (uint64_t)n) ++l;
+  return l;
 }
 
 // Neighbour tables: row-major nbr[n][27], or tile-major nbr[tile][27][128]
@@ -370,6 +431,7 @@ cudaError_t launch_conv_tc_bf16(const sc_map* m, const void* feats, const void* 
 bool conv_tc_supported(int cin, int cout);
 // Process-wide count of the kernels this library has launched (host side).
 void note_launches(int k);
+uint32_t* status_readback_buffer();  // pinned, kStatusBlockBytes, per host thread
 uint64_t launches();
 // Deterministic mode: the tensor-core kernel splits a unit in at most two
 // parts (a + b == b + a in fp32), so repeated calls are bit-identical.

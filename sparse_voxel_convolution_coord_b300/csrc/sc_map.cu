@@ -25,10 +25,12 @@
 //                    flight to hide the probe latency, which one thread per
 //                    voxel with 26 dependent resolutions could not.  The
 //                    tile-major output [tile][27][128] is written coalesced
-//                    (a warp writes 32 consecutive rows of one offset).  Each
+//                    (a warp writes 32 consecutive rows of one offset).  With
+//                    32-bit keys a lookup stops at its home slot unless that
+//                    slot's moved flag says a key homed there moved on.  Each
 //                    block ORs its rows' presence bits into the tile mask the
 //                    convolution uses to skip absent offsets, and adds its
-//                    pair count to a global counter.
+//                    pair count to one of 32 global counters.
 //  k_pairs_*         CSR pair lists per offset (ascending output row),
 //                    built on demand: count, scan, scatter.
 #include <algorithm>
@@ -42,6 +44,16 @@ constexpr int kInsertThreads = 256;
 // ---------------------------------------------------------------------------
 // insert
 
+// Key of a live slot.
+template <bool K32>
+__device__ __forceinline__ uint64_t slot_key(const HashParams& hp, unsigned long long s) {
+  if constexpr (K32)
+    return s >> 32;
+  else
+    return s >> hp.vbits;
+}
+
+template <bool K32>
 __global__ void __launch_bounds__(kInsertThreads) k_hash_insert(const int4* __restrict__ coords,
                                                                 HashParams hp, uint32_t* status) {
   const int lane = threadIdx.x & 31;
@@ -49,7 +61,7 @@ __global__ void __launch_bounds__(kInsertThreads) k_hash_insert(const int4* __re
   unsigned long long* slots = reinterpret_cast<unsigned long long*>(hp.slots);
   uint32_t err = 0;
   bool pending = false;
-  uint64_t key = 0, mine = 0, pos = 0, step = 0;
+  uint64_t key = 0, mine = 0, pos = 0, step = 0, home = 0;
   if (i < hp.n) {
     const int4 c = __ldg(coords + i);
     const bool in_range = c.x >= 0 && (unsigned)c.y < (unsigned)hp.res &&
@@ -58,6 +70,13 @@ __global__ void __launch_bounds__(kInsertThreads) k_hash_insert(const int4* __re
       err |= kStatRange;
     } else if ((uint64_t)c.x >= hp.bmax) {
       err |= kStatKeySpace;
+    } else if constexpr (K32) {
+      const uint32_t k32 = cell_key32(hp, c.x, c.y, c.z, c.w);
+      key = k32;
+      mine = ((uint64_t)k32 << 32) | (uint64_t)i;
+      pos = home_slot32(hp, c.x, c.y, c.z, c.w);
+      step = probe_step32(hp, k32);
+      pending = true;
     } else {
       key = cell_key(hp, c.x, c.y, c.z, c.w);
       mine = (key << hp.vbits) | (uint64_t)i;
@@ -65,6 +84,7 @@ __global__ void __launch_bounds__(kInsertThreads) k_hash_insert(const int4* __re
       step = probe_step(hp, key);
       pending = true;
     }
+    home = pos;
   }
   // Synchronous probing rounds; at most `capacity` rounds (every slot).
   for (uint64_t round = 0; __any_sync(0xffffffffu, pending); ++round) {
@@ -77,10 +97,12 @@ __global__ void __launch_bounds__(kInsertThreads) k_hash_insert(const int4* __re
     const unsigned long long old = atomicCAS(slots + pos, kEmptySlot, mine);
     if (old == kEmptySlot) {
       pending = false;
-    } else if ((old >> hp.vbits) == key) {
+    } else if (slot_key<K32>(hp, old) == key) {
       err |= kStatDuplicate;
       pending = false;
     } else {
+      // 32-bit keys: mark the home slot, whose key moved on.
+      if (K32 && round == 0) atomicOr(slots + home, (unsigned long long)kMovedFlag);
       pos = (pos + step) & hp.cap_mask;
     }
   }
@@ -113,7 +135,7 @@ __device__ __forceinline__ int32_t finish_probe(const HashParams& hp, uint64_t k
 // Grid (tiles, 9): block (t, col) resolves, for the 128 voxels of tile t,
 // the three neighbours (dz = -1, 0, 1) of neighbour column
 // col = 3 * (dx + 1) + (dy + 1), i.e. offsets k = 3 * col + {0, 1, 2}.
-template <NbrLayout L>
+template <NbrLayout L, bool K32>
 __global__ void __launch_bounds__(kTileRows) k_neighbor_query(
     const int4* __restrict__ coords, HashParams hp, int32_t* __restrict__ nbr,
     uint32_t* __restrict__ tile_mask, unsigned long long* pair_count) {
@@ -133,55 +155,111 @@ __global__ void __launch_bounds__(kTileRows) k_neighbor_query(
   // are +1, +2) and the groups of the two bricks along z that the three
   // cells fall in (bricks zb and zb + 1, zb = (z - 1) >> 1).
   const int zb = (c.w - 1) >> 1;
-  const uint64_t key_lo = cell_key(hp, c.x, x, y, c.w - 1);
-  const int64_t BR = hp.bres;
-  const int64_t brick_lo = (((int64_t)c.x * BR + (x >> 1)) * BR + (y >> 1)) * BR + zb;
-  const int gshift = 64 - (hp.log2cap - 3);
-  const uint64_t g_lo = ((uint64_t)brick_lo * 0x9E3779B97F4A7C15ull) >> gshift;
-  const uint64_t g_hi = ((uint64_t)(brick_lo + 1) * 0x9E3779B97F4A7C15ull) >> gshift;
-  const uint64_t cellxy = (uint64_t)(((x & 1) << 2) | ((y & 1) << 1));
-  unsigned long long s[3];
-  uint64_t home[3];
-  bool in[3];
+  int32_t r[3];
+  if constexpr (K32) {
+    const uint32_t key_lo = cell_key32(hp, c.x, x, y, c.w - 1);
+    uint32_t pos[3];
+    uint32_t pend = 0;  // lookups the home slot did not settle
+    const uint32_t BR = (uint32_t)hp.bres;
+    const uint32_t brick_lo =
+        (((uint32_t)c.x * BR + (uint32_t)(x >> 1)) * BR + (uint32_t)(y >> 1)) * BR + (uint32_t)zb;
+    const uint32_t g_lo = group32(hp, brick_lo), g_hi = group32(hp, brick_lo + 1u);
+    const uint32_t cellxy = (uint32_t)(((x & 1) << 2) | ((y & 1) << 1));
+    unsigned long long sl[3];
 #pragma unroll
-  for (int j = 0; j < 3; ++j) {
-    const int z = c.w + j - 1;
-    in[j] = colin && (unsigned)z < (unsigned)hp.res && !(col == 4 && j == 1);
-    home[j] = ((((z >> 1) != zb) ? g_hi : g_lo) << 3) | cellxy | (uint64_t)(z & 1);
-    s[j] = in[j] ? __ldg(slots + home[j]) : kEmptySlot;
+    for (int j = 0; j < 3; ++j) {
+      const int z = c.w + j - 1;
+      const bool in = colin && (unsigned)z < (unsigned)hp.res && !(col == 4 && j == 1);
+      pos[j] = (((z >> 1) != zb ? g_hi : g_lo) << 3) | cellxy | (uint32_t)(z & 1);
+      sl[j] = in ? __ldg(slots + pos[j]) : kEmptySlot;
+    }
+    // Home slots: the key, an empty slot, or another key with the moved
+    // flag clear all settle the lookup; otherwise it follows the probe
+    // sequence, the column's open lookups advancing together.
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      r[j] = -1;
+      if (sl[j] != kEmptySlot) {
+        if ((uint32_t)(sl[j] >> 32) == key_lo + (uint32_t)j)
+          r[j] = (int32_t)((uint32_t)sl[j] & kRowMask32);
+        else if (sl[j] & kMovedFlag)
+          pend |= 1u << j;
+      }
+    }
+    const uint32_t cmask = (uint32_t)hp.cap_mask;
+    for (uint32_t it = 0; pend != 0 && it < cmask; ++it) {
+#pragma unroll
+      for (int j = 0; j < 3; ++j)
+        if (pend & (1u << j)) {
+          pos[j] = (pos[j] + probe_step32(hp, key_lo + (uint32_t)j)) & cmask;
+          sl[j] = __ldg(slots + pos[j]);
+        }
+#pragma unroll
+      for (int j = 0; j < 3; ++j)
+        if (pend & (1u << j)) {
+          if (sl[j] == kEmptySlot) {
+            pend &= ~(1u << j);
+          } else if ((uint32_t)(sl[j] >> 32) == key_lo + (uint32_t)j) {
+            r[j] = (int32_t)((uint32_t)sl[j] & kRowMask32);
+            pend &= ~(1u << j);
+          }
+        }
+    }
+  } else {
+    const uint64_t key_lo = cell_key(hp, c.x, x, y, c.w - 1);
+    const int64_t BR = hp.bres;
+    const int64_t brick_lo = (((int64_t)c.x * BR + (x >> 1)) * BR + (y >> 1)) * BR + zb;
+    const int gshift = 64 - (hp.log2cap - 3);
+    const uint64_t g_lo = ((uint64_t)brick_lo * 0x9E3779B97F4A7C15ull) >> gshift;
+    const uint64_t g_hi = ((uint64_t)(brick_lo + 1) * 0x9E3779B97F4A7C15ull) >> gshift;
+    const uint64_t cellxy = (uint64_t)(((x & 1) << 2) | ((y & 1) << 1));
+    unsigned long long sl[3];
+    uint64_t home[3];
+    bool in[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int z = c.w + j - 1;
+      in[j] = colin && (unsigned)z < (unsigned)hp.res && !(col == 4 && j == 1);
+      home[j] = ((((z >> 1) != zb) ? g_hi : g_lo) << 3) | cellxy | (uint64_t)(z & 1);
+      sl[j] = in[j] ? __ldg(slots + home[j]) : kEmptySlot;
+    }
+#pragma unroll
+    for (int j = 0; j < 3; ++j)
+      r[j] = in[j] ? finish_probe(hp, key_lo + (uint64_t)j, home[j], sl[j]) : -1;
   }
   uint32_t bits = 0;
 #pragma unroll
   for (int j = 0; j < 3; ++j) {
     const int k = 3 * col + j;
-    int32_t r;
-    if (k == kCentre)
-      r = valid ? (int32_t)o : -1;
-    else
-      r = in[j] ? finish_probe(hp, key_lo + (uint64_t)j, home[j], s[j]) : -1;
-    bits |= (r >= 0 ? 1u : 0u) << k;
+    if (k == kCentre) r[j] = valid ? (int32_t)o : -1;
+    bits |= (r[j] >= 0 ? 1u : 0u) << k;
     if constexpr (L == kNbrTileMajor)
-      nbr[row0 * kTaps + k * kTileRows + threadIdx.x] = r;
+      nbr[row0 * kTaps + k * kTileRows + threadIdx.x] = r[j];
     else if (valid)
-      nbr[o * kTaps + k] = r;
+      nbr[o * kTaps + k] = r[j];
   }
+  const uint32_t cnt = (uint32_t)__popc(bits);
+  const int lane = threadIdx.x & 31;
+  // Per block: the offsets present in its rows into the tile mask (zeroed
+  // before the launch), its pair count into one of the counters (one
+  // atomic of each per block: per warp, the counters' L2 slice saturates).
   const uint32_t wor = __reduce_or_sync(0xffffffffu, bits);
-  const uint32_t wcnt = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(bits));
-  if ((threadIdx.x & 31) == 0) {
+  const uint32_t wcnt = __reduce_add_sync(0xffffffffu, cnt);
+  if (lane == 0) {
     s_or[threadIdx.x >> 5] = wor;
     s_cnt[threadIdx.x >> 5] = wcnt;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    uint32_t m = 0, cnt = 0;
+    uint32_t m = 0, bc = 0;
     for (int w = 0; w < kTileRows / 32; ++w) {
       m |= s_or[w];
-      cnt += s_cnt[w];
+      bc += s_cnt[w];
     }
-    if (m) atomicOr(tile_mask + blockIdx.x, m);  // zeroed before the launch
-    if (cnt)
+    if (m) atomicOr(tile_mask + blockIdx.x, m);
+    if (bc)
       atomicAdd(pair_count + (blockIdx.x * 9u + blockIdx.y) % kPairCounters,
-                (unsigned long long)cnt);
+                (unsigned long long)bc);
   }
 }
 
@@ -237,8 +315,12 @@ cudaError_t launch_hash_insert(const int32_t* coords, const HashParams& hp, uint
                                cudaStream_t s) {
   if (hp.n == 0) return cudaSuccess;
   const int64_t blocks = (hp.n + kInsertThreads - 1) / kInsertThreads;
-  k_hash_insert<<<(unsigned)blocks, kInsertThreads, 0, s>>>(reinterpret_cast<const int4*>(coords),
-                                                            hp, status);
+  if (hp.k32)
+    k_hash_insert<true><<<(unsigned)blocks, kInsertThreads, 0, s>>>(
+        reinterpret_cast<const int4*>(coords), hp, status);
+  else
+    k_hash_insert<false><<<(unsigned)blocks, kInsertThreads, 0, s>>>(
+        reinterpret_cast<const int4*>(coords), hp, status);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -251,10 +333,21 @@ cudaError_t launch_neighbor_query(const int32_t* coords, const HashParams& hp, i
   const int64_t tiles = (hp.n + kTileRows - 1) / kTileRows;
   const int4* c4 = reinterpret_cast<const int4*>(coords);
   const dim3 grid((unsigned)tiles, 9);
-  if (layout == kNbrTileMajor)
-    k_neighbor_query<kNbrTileMajor><<<grid, kTileRows, 0, s>>>(c4, hp, nbr, tile_mask, pair_count);
-  else
-    k_neighbor_query<kNbrRowMajor><<<grid, kTileRows, 0, s>>>(c4, hp, nbr, tile_mask, pair_count);
+  if (layout == kNbrTileMajor) {
+    if (hp.k32)
+      k_neighbor_query<kNbrTileMajor, true><<<grid, kTileRows, 0, s>>>(c4, hp, nbr, tile_mask,
+                                                                       pair_count);
+    else
+      k_neighbor_query<kNbrTileMajor, false><<<grid, kTileRows, 0, s>>>(c4, hp, nbr, tile_mask,
+                                                                        pair_count);
+  } else {
+    if (hp.k32)
+      k_neighbor_query<kNbrRowMajor, true><<<grid, kTileRows, 0, s>>>(c4, hp, nbr, tile_mask,
+                                                                      pair_count);
+    else
+      k_neighbor_query<kNbrRowMajor, false><<<grid, kTileRows, 0, s>>>(c4, hp, nbr, tile_mask,
+                                                                       pair_count);
+  }
   note_launches(1);
   return cudaGetLastError();
 }

@@ -77,33 +77,18 @@ extern "C" SC_API sc_status sc_build_neighbor_table_noalloc(const int32_t* coord
     return report(SC_ERR_INVALID_ARG,
                   "sc_build_neighbor_table_noalloc: coords and nbr_out must be 16-byte aligned "
                   "device pointers");
-  const int vbits = 64 - __builtin_clzll((unsigned long long)n);
-  const uint64_t res3 = (uint64_t)res * res * res;
-  const uint64_t bmax = (1ull << (64 - vbits)) / res3;
-  if (bmax == 0)
-    return report(SC_ERR_UNSUPPORTED,
-                  "sc_build_neighbor_table_noalloc: res=%lld too large for the hash key", res);
-
   uint64_t* scratch = nullptr;
   cudaError_t e = scratch_on_current_device(&scratch);
   if (e != cudaSuccess)
     return report(SC_ERR_CUDA, "sc_build_neighbor_table_noalloc: scratch lookup failed (%lld)",
                   (long long)e);
-  uint64_t cap = 64;
-  int log2cap = 6;
-  while (cap < 2ull * (uint64_t)n) {
-    cap <<= 1;
-    ++log2cap;
-  }
+  // Load factor <= 1/4 where the static table allows, <= 1/2 always.
+  int log2cap = sc::hash_log2cap(n);
+  while ((1ull << log2cap) > kNoAllocSlots) --log2cap;
   sc::HashParams hp;
-  hp.slots = scratch;
-  hp.cap_mask = cap - 1;
-  hp.log2cap = log2cap;
-  hp.vbits = vbits;
-  hp.res = res;
-  hp.bres = (res + 1) / 2;
-  hp.bmax = bmax;
-  hp.n = n;
+  if (!sc::make_hash_params(hp, scratch, n, res, log2cap, true))
+    return report(SC_ERR_UNSUPPORTED,
+                  "sc_build_neighbor_table_noalloc: res=%lld too large for the hash key", res);
   uint32_t* tile_mask = reinterpret_cast<uint32_t*>(scratch + kMaskWordOffset);
   uint32_t* status = reinterpret_cast<uint32_t*>(scratch + kStatusWordOffset);
   unsigned long long* pair_count = reinterpret_cast<unsigned long long*>(status + 4);
@@ -112,14 +97,26 @@ extern "C" SC_API sc_status sc_build_neighbor_table_noalloc(const int32_t* coord
   // The scratch keeps the previous call's contents: clear the slots in use and
   // the status / pair-count words.
   const int64_t ntiles = (n + sc::kTileRows - 1) / sc::kTileRows;
-  e = sc::launch_map_init(hp, tile_mask, ntiles, status, s);
-  if (e == cudaSuccess) e = sc::launch_hash_insert(coords, hp, status, s);
-  if (e == cudaSuccess)
-    e = sc::launch_neighbor_query(coords, hp, nbr_out, tile_mask, pair_count, status,
-                                  sc::kNbrRowMajor, s);
-  uint32_t host[sc::kStatusBlockBytes / 4] = {};
-  if (e == cudaSuccess) e = cudaMemcpyAsync(host, status, sizeof(host), cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  // As sc_build_map: a batch index beyond the 32-bit key space is retried
+  // once with 64-bit keys.
+  uint32_t host_local[sc::kStatusBlockBytes / 4] = {};
+  uint32_t* host = sc::status_readback_buffer();
+  if (!host) host = host_local;
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    e = sc::launch_map_init(hp, tile_mask, ntiles, status, s);
+    if (e == cudaSuccess) e = sc::launch_hash_insert(coords, hp, status, s);
+    if (e == cudaSuccess)
+      e = sc::launch_neighbor_query(coords, hp, nbr_out, tile_mask, pair_count, status,
+                                    sc::kNbrRowMajor, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(host, status, sc::kStatusBlockBytes, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess || !hp.k32 || !(host[0] & sc::kStatKeySpace) ||
+        (host[0] & sc::kStatRange))
+      break;
+    if (!sc::make_hash_params(hp, scratch, n, res, log2cap, false)) break;
+  }
+  const uint64_t bmax = hp.bmax;
   if (e != cudaSuccess)
     return report(SC_ERR_CUDA, "sc_build_neighbor_table_noalloc: CUDA error %lld", (long long)e);
   const uint32_t st = host[0];

@@ -107,7 +107,8 @@ def test_map_shuffled_and_repeatable(sc):
 
 
 @pytest.mark.parametrize("case", ["full_cube", "res1_batches", "batch_gaps", "single",
-                                  "line_z", "sparse_big_res"])
+                                  "line_z", "sparse_big_res", "k32_last_batch",
+                                  "k32_overflow_retry"])
 def test_map_edge_cases(sc, case):
     rng = np.random.default_rng(2)
     if case == "full_cube":
@@ -122,6 +123,12 @@ def test_map_edge_cases(sc, case):
         coords, res = np.array([[2, 5, 0, 7]], np.int32), 8
     elif case == "line_z":
         coords, res = np.array([[0, 3, 3, z] for z in range(300)], np.int32), 300
+    elif case == "k32_last_batch":
+        # res 64: 32-bit keys hold batch indices < (2^32 - 1) // 64^3 = 16383
+        coords, res = random_coords(rng, 0, 64, 0.01, batch_ids=[0, 16382]), 64
+    elif case == "k32_overflow_retry":
+        # batch 16383 reaches key 2^32 - 1 and 20000 lies beyond: 64-bit keys
+        coords, res = random_coords(rng, 0, 64, 0.01, batch_ids=[0, 16383, 20000]), 64
     else:
         coords, res = random_coords(rng, 1, 64, 0.002), 1 << 14
         coords[:, 1:] *= 200

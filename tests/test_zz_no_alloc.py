@@ -57,7 +57,7 @@ def allocating_table(coords_dev, res):
 
 def test_noalloc_matches_allocating_path_twice(lib):
     import sparse_voxel_convolution_coord_b300 as sc
-    for key in (3, 2):        # 29,850 voxels, then 20,236 over the same scratch
+    for key in (5, 3, 2):     # 395,775, 29,850, then 20,236 voxels over the same scratch
         p = synth.make_problem(key)
         coords = torch.from_numpy(p.coords).cuda()
         rc, nbr, pairs = noalloc_table(lib, coords, p.res)
@@ -65,6 +65,24 @@ def test_noalloc_matches_allocating_path_twice(lib):
         want, want_pairs = allocating_table(coords, p.res)
         np.testing.assert_array_equal(nbr, want)
         assert pairs == want_pairs
+
+
+def test_noalloc_key_space_retry(lib):
+    """Batch indices beyond the 32-bit key space at res 64 (>= 16383) make the
+    build retry with 64-bit keys; the table still matches the allocating path."""
+    import sparse_voxel_convolution_coord_b300 as sc
+    rng = np.random.default_rng(11)
+    rows = []
+    for b in (0, 16383, 20000):
+        xyz = np.argwhere(rng.random((64, 64, 64)) < 0.01)
+        rows.append(np.concatenate([np.full((len(xyz), 1), b), xyz], axis=1))
+    # argwhere's rows are column-major: make them C-contiguous for the raw call
+    coords = torch.from_numpy(np.ascontiguousarray(np.concatenate(rows), dtype=np.int32)).cuda()
+    rc, nbr, pairs = noalloc_table(lib, coords, 64)
+    assert rc == sc.SC_OK, sc.sc_last_error_msg()
+    want, want_pairs = allocating_table(coords, 64)
+    np.testing.assert_array_equal(nbr, want)
+    assert pairs == want_pairs
 
 
 def test_noalloc_rejects_beyond_limit_and_reports_errors(lib):
