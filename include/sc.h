@@ -64,6 +64,13 @@ typedef enum {
 
 typedef enum { SC_F32 = 0, SC_BF16 = 1 } sc_dtype;
 
+/* Activation of the fused epilogue (sc_forward_ex). */
+typedef enum {
+  SC_ACT_NONE = 0,
+  SC_ACT_RELU = 1, /* max(v, 0)                  */
+  SC_ACT_SILU = 2  /* v * sigmoid(v) = v / (1 + e^-v) */
+} sc_activation;
+
 /*
  * Build the coordinate hash table and the neighbour map of N active voxels
  * ("Porting TRELLIS.2 ...", section V: the neighbour table is built once per
@@ -122,6 +129,31 @@ SC_API sc_handle sc_build_map(const int32_t* coords, int64_t n, int32_t res, voi
  */
 SC_API sc_status sc_forward(sc_handle h, const void* feats, const void* weight, const float* bias,
                      float* out, int32_t cin, int32_t cout, sc_dtype dtype, void* stream);
+
+/*
+ * sc_forward with the whole epilogue fused into the same pass ("Porting
+ * TRELLIS.2 ...", section V: bias, rounding, activation and the residual add
+ * fused into the convolution's output pass):
+ *   out[o][:] = act(acc[o][:] + bias[:]) + residual[o][:]
+ * computed in fp32 (acc = the sum over offsets above) and stored once in
+ * out_dtype, bf16 by rounding to nearest, ties to even.  The pages fix
+ * neither the activation nor the order; the activation is applied to the
+ * convolution's output and the residual (a skip connection) added after it.
+ *
+ *   residual  device [n][cout] in out_dtype, 16-byte aligned, or NULL.
+ *   out       device [n][cout] in out_dtype, 16-byte aligned; fully written.
+ *   act       SC_ACT_NONE, SC_ACT_RELU or SC_ACT_SILU.
+ *   out_dtype SC_F32 or SC_BF16 (either with either input dtype).
+ * sc_forward(...) is sc_forward_ex(..., NULL residual, SC_ACT_NONE, SC_F32).
+ * On the SC_BF16 path an activation or a bf16 output turns the tail split
+ * (see sc_forward) off, since neither can be applied to a partial sum; a
+ * residual alone keeps it (the last part adds it).
+ * Errors as sc_forward, plus SC_ERR_INVALID_ARG for a bad act or out_dtype.
+ */
+SC_API sc_status sc_forward_ex(sc_handle h, const void* feats, const void* weight,
+                               const float* bias, const void* residual, void* out, int32_t cin,
+                               int32_t cout, sc_dtype dtype, sc_activation act, sc_dtype out_dtype,
+                               void* stream);
 
 /*
  * Release a map.  Its device memory is freed in stream order on `stream`:

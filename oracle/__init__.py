@@ -13,7 +13,10 @@ Sources followed (page title, section):
   * "Porting TRELLIS.2 From Python to Rust and Metal", section V -- neighbour
     table built once per level, gather-GEMM, bias in the same pass;
   * "FABLE_STARTUP_PACKET.md", section 5 -- weights (Co,Kd,Kh,Kw,Ci) viewed as
-    (Kvol, Ci, Co).
+    (Kvol, Ci, Co);
+  * "Porting TRELLIS.2 From Python to Rust and Metal", section V -- bias,
+    rounding, activation and the residual add fused into the output pass
+    (``epilogue`` and ``round_bf16`` below, plain numpy in fp64).
 
 Every function below is pinned by ``tests/test_oracle_pins.py`` against
 routes that do not go through this code: brute-force neighbour search, a
@@ -25,6 +28,7 @@ import numpy as np
 from . import build_oracle
 
 OK, BAD_ARG, COORD_RANGE, DUPLICATE = 0, 1, 2, 3
+ACT_NONE, ACT_RELU, ACT_SILU = 0, 1, 2
 
 
 class OracleError(RuntimeError):
@@ -147,3 +151,55 @@ def sparse_conv(coords, res, feats, weight, bias=None, threads=0):
 
 def max_threads():
     return default().max_threads()
+
+
+# ---------------------------------------------------------------------------
+# Fused epilogue ("Porting TRELLIS.2 From Python to Rust and Metal", section
+# V: bias, rounding, activation and the residual add in the convolution's
+# output pass).  The pages name neither the activation nor the order; the
+# reading taken: out = act(conv + bias) + residual, then one rounding to the
+# output type.
+
+
+def activation(v, act):
+    """fp64 activation: identity, ReLU max(v, 0), or SiLU v * sigmoid(v)."""
+    v = np.asarray(v, dtype=np.float64)
+    if act == ACT_NONE:
+        return v.copy()
+    if act == ACT_RELU:
+        return np.where(v > 0.0, v, 0.0)
+    if act == ACT_SILU:
+        # v / (1 + e^-v); for v < 0 written as v e^v / (1 + e^v) so that
+        # e^-v cannot overflow
+        e = np.exp(-np.abs(v))
+        return np.where(v >= 0.0, v / (1.0 + e), v * e / (1.0 + e))
+    raise ValueError("unknown activation %r" % (act,))
+
+
+def epilogue(conv_out, act=ACT_NONE, residual=None):
+    """act(conv_out) + residual in fp64; conv_out already holds the bias."""
+    y = activation(conv_out, act)
+    if residual is not None:
+        y = y + np.asarray(residual, dtype=np.float64)
+    return y
+
+
+def round_bf16(v):
+    """Round fp64 values to bfloat16 (8 significant bits, fp32's exponent
+    range), nearest with ties to even; returned as fp64.  Written from the
+    format's definition: v = m * 2^e with 0.5 <= |m| < 1 keeps m to 8 bits,
+    i.e. v is rounded to a multiple of 2^(e - 8); below fp32's normal range
+    (2^-126) the spacing stays 2^-133.  Values past the largest finite bf16
+    become infinities."""
+    v = np.asarray(v, dtype=np.float64)
+    out = np.zeros_like(v)
+    nz = (v != 0.0) & np.isfinite(v)
+    _, e = np.frexp(v[nz])
+    e = np.maximum(e, -125)
+    step = np.ldexp(1.0, e - 8)
+    q = np.rint(v[nz] / step) * step  # rint: round half to even
+    big = np.abs(q) > float.fromhex("0x1.fep127")
+    q[big] = np.copysign(np.inf, q[big])
+    out[nz] = q
+    out[~nz] = v[~nz]
+    return out

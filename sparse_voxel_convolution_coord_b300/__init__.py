@@ -24,6 +24,7 @@ __all__ = [
     "sc_last_error_msg", "sc_version", "sc_set_deterministic", "sc_kernel_launches", "SC_OK", "SC_ERR_INVALID_ARG", "SC_ERR_COORD_RANGE",
     "SC_ERR_DUPLICATE", "SC_ERR_TABLE_FULL", "SC_ERR_UNSUPPORTED", "SC_ERR_ALLOC",
     "SC_ERR_CUDA", "SC_ERR_BAD_HANDLE", "SC_ERR_DEVICE_TIMEOUT", "SC_F32", "SC_BF16",
+    "SC_ACT_NONE", "SC_ACT_RELU", "SC_ACT_SILU", "sc_forward_ex",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -34,6 +35,8 @@ HEADER = os.path.join(_ROOT, "include", "sc.h")
  SC_ERR_UNSUPPORTED, SC_ERR_ALLOC, SC_ERR_CUDA, SC_ERR_BAD_HANDLE,
  SC_ERR_DEVICE_TIMEOUT) = range(10)
 SC_F32, SC_BF16 = 0, 1
+SC_ACT_NONE, SC_ACT_RELU, SC_ACT_SILU = 0, 1, 2
+_ACTS = {"none": SC_ACT_NONE, "relu": SC_ACT_RELU, "silu": SC_ACT_SILU}
 
 _lib = None
 
@@ -69,6 +72,9 @@ def load_library():
     lib.sc_build_map.restype = P
     lib.sc_forward.argtypes = [P, P, P, P, P, I32, I32, ctypes.c_int, P]
     lib.sc_forward.restype = ctypes.c_int
+    lib.sc_forward_ex.argtypes = [P, P, P, P, P, P, I32, I32, ctypes.c_int, ctypes.c_int,
+                                  ctypes.c_int, P]
+    lib.sc_forward_ex.restype = ctypes.c_int
     lib.sc_free_map.argtypes = [P, P]
     lib.sc_free_map.restype = ctypes.c_int
     lib.sc_map_size.argtypes = [P]
@@ -228,6 +234,50 @@ def sc_forward(m: Map, feats, weight, bias=None, out=None, stream=None):
     rc = load_library().sc_forward(ctypes.c_void_p(m.ptr), _dev_ptr(feats, "feats"),
                                    _dev_ptr(weight, "weight"), _dev_ptr(bias, "bias"),
                                    _dev_ptr(out, "out"), cin, cout, dt, _stream_ptr(stream))
+    _check(rc)
+    return out
+
+
+def sc_forward_ex(m: Map, feats, weight, bias=None, residual=None, act="none",
+                  out_dtype=None, out=None, stream=None):
+    """Convolution with the fused epilogue: out = act(conv + bias) + residual.
+
+    act is "none", "relu" or "silu"; out_dtype torch.float32 (default) or
+    torch.bfloat16; residual [N,cout] in out_dtype or None.  Asynchronous.
+    """
+    import torch
+    if feats.dtype != weight.dtype:
+        raise ValueError("feats and weight must have the same dtype")
+    if feats.dtype == torch.bfloat16:
+        dt = SC_BF16
+    elif feats.dtype == torch.float32:
+        dt = SC_F32
+    else:
+        raise ValueError("dtype must be bfloat16 or float32")
+    if act not in _ACTS:
+        raise ValueError("act must be one of %s" % sorted(_ACTS))
+    out_dtype = torch.float32 if out_dtype is None else out_dtype
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("out_dtype must be float32 or bfloat16")
+    odt = SC_BF16 if out_dtype == torch.bfloat16 else SC_F32
+    n, cin = feats.shape
+    if weight.dim() != 3 or weight.shape[0] != 27 or weight.shape[1] != cin:
+        raise ValueError("weight must be [27, cin, cout]")
+    cout = weight.shape[2]
+    if n != m.n:
+        raise ValueError("feats has %d rows, the map %d" % (n, m.n))
+    if bias is not None and (bias.dtype != torch.float32 or bias.numel() != cout):
+        raise ValueError("bias must be fp32 [cout]")
+    if residual is not None and (residual.dtype != out_dtype or tuple(residual.shape) != (n, cout)):
+        raise ValueError("residual must be [N, cout] in out_dtype")
+    if out is None:
+        out = torch.empty((n, cout), dtype=out_dtype, device=feats.device)
+    elif out.dtype != out_dtype or tuple(out.shape) != (n, cout):
+        raise ValueError("out must be [N, cout] in out_dtype")
+    rc = load_library().sc_forward_ex(
+        ctypes.c_void_p(m.ptr), _dev_ptr(feats, "feats"), _dev_ptr(weight, "weight"),
+        _dev_ptr(bias, "bias"), _dev_ptr(residual, "residual"), _dev_ptr(out, "out"), cin, cout,
+        dt, _ACTS[act], odt, _stream_ptr(stream))
     _check(rc)
     return out
 

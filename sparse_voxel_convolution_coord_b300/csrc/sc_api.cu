@@ -357,10 +357,21 @@ sc_status sc_get_pairs(sc_handle h, int64_t* off_host, int32_t* in, int32_t* out
 
 sc_status sc_forward(sc_handle h, const void* feats, const void* weight, const float* bias,
                      float* out, int32_t cin, int32_t cout, sc_dtype dtype, void* stream) {
+  return sc_forward_ex(h, feats, weight, bias, nullptr, out, cin, cout, dtype, SC_ACT_NONE, SC_F32,
+                       stream);
+}
+
+sc_status sc_forward_ex(sc_handle h, const void* feats, const void* weight, const float* bias,
+                        const void* residual, void* out, int32_t cin, int32_t cout,
+                        sc_dtype dtype, sc_activation act, sc_dtype out_dtype, void* stream) {
   if (!is_live(h)) return fail(SC_ERR_BAD_HANDLE, "sc_forward: handle is not live");
   if (cin < 1 || cout < 1) return fail(SC_ERR_INVALID_ARG, "sc_forward: cin/cout must be >= 1");
   if (dtype != SC_F32 && dtype != SC_BF16)
     return fail(SC_ERR_UNSUPPORTED, "sc_forward: dtype %d not supported", (int)dtype);
+  if (out_dtype != SC_F32 && out_dtype != SC_BF16)
+    return fail(SC_ERR_INVALID_ARG, "sc_forward_ex: out_dtype %d not supported", (int)out_dtype);
+  if (act != SC_ACT_NONE && act != SC_ACT_RELU && act != SC_ACT_SILU)
+    return fail(SC_ERR_INVALID_ARG, "sc_forward_ex: activation %d not supported", (int)act);
   if (dtype == SC_BF16 && !sc::conv_tc_supported(cin, cout))
     return fail(SC_ERR_UNSUPPORTED,
                 "sc_forward: bf16 needs cin in {16,32} or a multiple of 64 <= 1024 and cout a "
@@ -372,20 +383,27 @@ sc_status sc_forward(sc_handle h, const void* feats, const void* weight, const f
   if (!feats || !weight || !out)
     return fail(SC_ERR_INVALID_ARG, "sc_forward: feats, weight and out must be non-NULL");
   if (!aligned(feats, 16) || !aligned(weight, 16) || !aligned(out, 16) ||
-      (bias && !aligned(bias, 4)))
-    return fail(SC_ERR_INVALID_ARG, "sc_forward: feats/weight/out must be 16-byte aligned");
+      (residual && !aligned(residual, 16)) || (bias && !aligned(bias, 4)))
+    return fail(SC_ERR_INVALID_ARG,
+                "sc_forward: feats/weight/out/residual must be 16-byte aligned");
   int dev = -1;
   cudaGetDevice(&dev);
   if (dev != h->device)
     return fail(SC_ERR_INVALID_ARG, "sc_forward: map lives on device %d, current is %d",
                 h->device, dev);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  sc::Epilogue ep;
+  ep.bias = bias;
+  ep.residual = residual;
+  ep.out = out;
+  ep.act = (int)act;
+  ep.out_bf16 = out_dtype == SC_BF16 ? 1 : 0;
   cudaError_t e;
   if (dtype == SC_BF16)
-    e = sc::launch_conv_tc_bf16(h, feats, weight, bias, out, cin, cout, s);
+    e = sc::launch_conv_tc_bf16(h, feats, weight, ep, cin, cout, s);
   else
     e = sc::launch_conv_simt_f32(h, static_cast<const float*>(feats),
-                                 static_cast<const float*>(weight), bias, out, cin, cout, s);
+                                 static_cast<const float*>(weight), ep, cin, cout, s);
   if (e != cudaSuccess) return fail_cuda(e, "sc_forward");
   return ok();
 }

@@ -12,7 +12,10 @@
 // then, for each offset present in any of the block's rows, the W[k] slice
 // (32 rows x cout) is staged in shared memory by cp.async, double-buffered one
 // offset ahead, and shared by the 8 warps.  Each output row is written once,
-// no atomics.
+// no atomics, through the fused epilogue (activation, residual, fp32 or bf16
+// output).
+#include <cuda_bf16.h>
+
 #include "sc_internal.cuh"
 
 namespace sc {
@@ -31,8 +34,7 @@ __device__ __forceinline__ void cp_async_16_ca(void* dst, const void* src) {
 template <int J>  // columns per lane = J, cout <= 32 * J
 __global__ void __launch_bounds__(kSimtWarps * 32) k_conv_simt_f32(
     const int32_t* __restrict__ nbr, int64_t n, const float* __restrict__ feats,
-    const float* __restrict__ w, const float* __restrict__ bias, float* __restrict__ out, int cin,
-    int cout) {
+    const float* __restrict__ w, const Epilogue ep, int cin, int cout) {
   __shared__ float s_a[kSimtWarps][kTaps][32];
   __shared__ uint32_t s_mask[kSimtWarps];
   extern __shared__ __align__(16) float s_w[];  // [2][32][32 * J]
@@ -114,14 +116,24 @@ __global__ void __launch_bounds__(kSimtWarps * 32) k_conv_simt_f32(
 #pragma unroll
     for (int j = 0; j < J; ++j) {
       const int c = lane + 32 * j;
-      if (c < cout) out[o * cout + c] = acc[j] + (bias ? __ldg(bias + c) : 0.f);
+      if (c >= cout) continue;
+      const int64_t e = o * cout + c;
+      float v = apply_act(acc[j] + (ep.bias ? __ldg(ep.bias + c) : 0.f), ep.act);
+      if (ep.out_bf16) {
+        if (ep.residual)
+          v += __bfloat162float(static_cast<const __nv_bfloat16*>(ep.residual)[e]);
+        static_cast<__nv_bfloat16*>(ep.out)[e] = __float2bfloat16_rn(v);
+      } else {
+        if (ep.residual) v += __ldg(static_cast<const float*>(ep.residual) + e);
+        static_cast<float*>(ep.out)[e] = v;
+      }
     }
   }
 }
 
 template <int J>
-cudaError_t launch_simt(const sc_map* m, const float* feats, const float* w, const float* bias,
-                        float* out, int cin, int cout, cudaStream_t s) {
+cudaError_t launch_simt(const sc_map* m, const float* feats, const float* w, const Epilogue& ep,
+                        int cin, int cout, cudaStream_t s) {
   const size_t smem = 2ull * 32 * 32 * J * sizeof(float);
   static bool attr = false;  // opt-in above 48 KB of dynamic shared memory
   if (!attr) {
@@ -131,20 +143,18 @@ cudaError_t launch_simt(const sc_map* m, const float* feats, const float* w, con
     attr = true;
   }
   const unsigned blocks = (unsigned)((m->n + kSimtWarps - 1) / kSimtWarps);
-  k_conv_simt_f32<J><<<blocks, kSimtWarps * 32, smem, s>>>(m->nbr, m->n, feats, w, bias, out, cin,
-                                                           cout);
+  k_conv_simt_f32<J><<<blocks, kSimtWarps * 32, smem, s>>>(m->nbr, m->n, feats, w, ep, cin, cout);
   note_launches(1);
   return cudaGetLastError();
 }
 
 cudaError_t launch_conv_simt_f32(const sc_map* m, const float* feats, const float* w,
-                                 const float* bias, float* out, int cin, int cout,
-                                 cudaStream_t s) {
+                                 const Epilogue& ep, int cin, int cout, cudaStream_t s) {
   const int J = (cout + 31) / 32;
-  if (J <= 1) return launch_simt<1>(m, feats, w, bias, out, cin, cout, s);
-  if (J <= 2) return launch_simt<2>(m, feats, w, bias, out, cin, cout, s);
-  if (J <= 4) return launch_simt<4>(m, feats, w, bias, out, cin, cout, s);
-  return launch_simt<8>(m, feats, w, bias, out, cin, cout, s);
+  if (J <= 1) return launch_simt<1>(m, feats, w, ep, cin, cout, s);
+  if (J <= 2) return launch_simt<2>(m, feats, w, ep, cin, cout, s);
+  if (J <= 4) return launch_simt<4>(m, feats, w, ep, cin, cout, s);
+  return launch_simt<8>(m, feats, w, ep, cin, cout, s);
 }
 
 }  // namespace sc

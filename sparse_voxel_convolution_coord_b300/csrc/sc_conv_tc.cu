@@ -131,7 +131,10 @@ struct TcArgs {
   const int32_t* nbr;          // tile-major [ntiles][27][128], pad rows -1
   const uint32_t* tile_mask;   // [ntiles]
   const float* bias;
-  float* out;
+  const void* residual;  // [n][cout] in the output dtype, or nullptr
+  void* out;             // fp32 or bf16 [n][cout]
+  int act;               // fused activation (SC_ACT_*)
+  int out_bf16;          // bf16 output (round to nearest even)
   uint32_t* status;
   int64_t n;
   int64_t ntiles;
@@ -557,9 +560,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                    unit_stages<CS>(unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles), p.cin), s0, s1);
         if (s0 == s1) continue;
       }
-      // Whole units store; parts add into the zeroed rows, the last with the bias.
+      // Whole units store; parts add into the zeroed rows, the last with the
+      // bias and the residual.  (The host never splits with an activation or
+      // a bf16 output.)
       const bool add = wi.part >= 0;
-      const float bscale = (wi.part < p.split - 1) && add ? 0.f : 1.f;
+      const bool last = !add || wi.part == p.split - 1;
+      const float bscale = last ? 1.f : 0.f;
+      const bool resid = p.residual != nullptr && last;
+      const int64_t wrow0 = (wi.unit * CL + rank) * kTileRows + warp * 32;  // this warp's rows
+      if (resid && wrow0 + lane < p.n) {
+        // This thread's row of the residual into L2 while the main loop runs
+        // (128-byte lines); the column-group loads below then hit L2.
+        const int rbytes = p.cout * (p.out_bf16 ? 2 : 4);
+        const char* rrow = static_cast<const char*>(p.residual) + (wrow0 + lane) * rbytes;
+        for (int off = 0; off < rbytes; off += 128)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(rrow + off));
+      }
       if (add && !rows_zeroed) {
         asm volatile("griddepcontrol.wait;" ::: "memory");
         rows_zeroed = true;
@@ -569,7 +585,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      const int64_t wrow0 = (wi.unit * CL + rank) * kTileRows + warp * 32;  // this warp's rows
       const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + acc * NPAD;
       float* stg = s_epi + warp * (32 * kStageRow);
       for (int ch = 0; ch < nchunks; ++ch) {
@@ -589,19 +604,69 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
         // ... and out again by column groups: each store instruction writes
-        // four rows x 128 contiguous bytes.
+        // four rows x 128 contiguous bytes (64 for bf16), after the rest of
+        // the epilogue (activation, residual, rounding).
+        // Two halves of four column groups; each half's residual values are
+        // loaded before any of its stores (out and residual may alias, so a
+        // load cannot move past a store).  Four, not eight, at a time: the
+        // kernel's 14 warps leave 128 registers a thread.
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int r = 4 * q + (lane >> 3), g = lane & 7;
-          const int c = ch * 32 + 4 * g;
-          const int64_t row = wrow0 + r;
-          const float4 o = *reinterpret_cast<const float4*>(stg + r * kStageRow + 4 * g);
-          if (row < p.n && c < p.cout) {
-            float4* dst = reinterpret_cast<float4*>(p.out + row * p.cout + c);
-            if (add)
-              atomicAdd(dst, o);
-            else
-              __stcs(dst, o);
+        for (int h = 0; h < 2; ++h) {
+          float4 rv[4];
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            const int q = 4 * h + qq;
+            const int r = 4 * q + (lane >> 3), c = ch * 32 + 4 * (lane & 7);
+            const int64_t row = wrow0 + r;
+            rv[qq] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (resid && row < p.n && c < p.cout) {
+              const int64_t e = row * p.cout + c;
+              if (p.out_bf16) {
+                const uint2 rb = __ldg(reinterpret_cast<const uint2*>(
+                    static_cast<const __nv_bfloat16*>(p.residual) + e));
+                rv[qq].x = __uint_as_float(rb.x << 16);  // bf16 -> fp32 is exact: the high half
+                rv[qq].y = __uint_as_float(rb.x & 0xffff0000u);
+                rv[qq].z = __uint_as_float(rb.y << 16);
+                rv[qq].w = __uint_as_float(rb.y & 0xffff0000u);
+              } else {
+                rv[qq] = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.residual) + e));
+              }
+            }
+          }
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            const int q = 4 * h + qq;
+            const int r = 4 * q + (lane >> 3), g = lane & 7;
+            const int c = ch * 32 + 4 * g;
+            const int64_t row = wrow0 + r;
+            float4 o = *reinterpret_cast<const float4*>(stg + r * kStageRow + 4 * g);
+            if (row < p.n && c < p.cout) {
+              const int64_t e = row * p.cout + c;
+              if (p.act) {
+                o.x = apply_act(o.x, p.act);
+                o.y = apply_act(o.y, p.act);
+                o.z = apply_act(o.z, p.act);
+                o.w = apply_act(o.w, p.act);
+              }
+              o.x += rv[qq].x;
+              o.y += rv[qq].y;
+              o.z += rv[qq].z;
+              o.w += rv[qq].w;
+              if (p.out_bf16) {
+                const __nv_bfloat162 b01 = __float22bfloat162_rn(make_float2(o.x, o.y));
+                const __nv_bfloat162 b23 = __float22bfloat162_rn(make_float2(o.z, o.w));
+                uint2 pk;
+                pk.x = *reinterpret_cast<const uint32_t*>(&b01);
+                pk.y = *reinterpret_cast<const uint32_t*>(&b23);
+                __stcs(reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + e), pk);
+              } else {
+                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + e);
+                if (add)
+                  atomicAdd(dst, o);
+                else
+                  __stcs(dst, o);
+              }
+            }
           }
         }
         __syncwarp();
@@ -715,8 +780,8 @@ int tail_split(int64_t nunits, int64_t G, int max_stages) {
 }
 
 template <int NPAD, int CS, int CL>
-cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, const float* bias,
-                         float* out, int cin, int cout, cudaStream_t s) {
+cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, const Epilogue& ep,
+                         int cin, int cout, cudaStream_t s) {
   using C = TcCfg<NPAD, CS>;
   auto kern = k_conv_tc<NPAD, CS, CL>;
   static LaunchCache cache;
@@ -767,8 +832,11 @@ cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, cons
   a.feats = static_cast<const __nv_bfloat16*>(feats);
   a.nbr = m->nbr;
   a.tile_mask = m->tile_mask;
-  a.bias = bias;
-  a.out = out;
+  a.bias = ep.bias;
+  a.residual = ep.residual;
+  a.out = ep.out;
+  a.act = ep.act;
+  a.out_bf16 = ep.out_bf16;
   a.status = m->d_status;
   a.n = m->n;
   a.ntiles = m->ntiles;
@@ -777,7 +845,8 @@ cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, cons
   const int64_t nunits = (m->ntiles + CL - 1) / CL;
   if (nunits == 0) return cudaSuccess;
   const int max_stages = CS == 64 ? kTaps * (cin / 64) : (kTaps + 64 / CS - 1) / (64 / CS);
-  const int split = tail_split(nunits, max_clusters, max_stages);
+  // An activation or a bf16 output cannot be applied to partial sums.
+  const int split = (ep.act || ep.out_bf16) ? 1 : tail_split(nunits, max_clusters, max_stages);
   a.split = split;
   a.tail = split > 1 ? (nunits >= max_clusters ? nunits % max_clusters : nunits) : 0;
   a.whole = nunits - a.tail;
@@ -789,7 +858,8 @@ cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, cons
     const int64_t row0 = a.whole * CL * kTileRows;
     const int64_t n4 = (m->n - row0) * cout / 4;  // cout is a multiple of 16
     const int64_t zb = std::min<int64_t>((n4 + 255) / 256, 2 * 148);
-    k_zero_rows<<<(unsigned)zb, 256, 0, s>>>(reinterpret_cast<float4*>(out + row0 * cout), n4);
+    k_zero_rows<<<(unsigned)zb, 256, 0, s>>>(
+        reinterpret_cast<float4*>(static_cast<float*>(ep.out) + row0 * cout), n4);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     note_launches(1);
@@ -803,19 +873,18 @@ cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, cons
 }
 
 template <int NPAD, int CS>
-cudaError_t launch_cl(const sc_map* m, const void* feats, const void* w, const float* bias,
-                      float* out, int cin, int cout, cudaStream_t s) {
-  if (cluster_size(NPAD) == 2)
-    return launch_typed<NPAD, CS, 2>(m, feats, w, bias, out, cin, cout, s);
-  return launch_typed<NPAD, CS, 1>(m, feats, w, bias, out, cin, cout, s);
+cudaError_t launch_cl(const sc_map* m, const void* feats, const void* w, const Epilogue& ep,
+                      int cin, int cout, cudaStream_t s) {
+  if (cluster_size(NPAD) == 2) return launch_typed<NPAD, CS, 2>(m, feats, w, ep, cin, cout, s);
+  return launch_typed<NPAD, CS, 1>(m, feats, w, ep, cin, cout, s);
 }
 
 template <int NPAD>
-cudaError_t launch_npad(const sc_map* m, const void* feats, const void* w, const float* bias,
-                        float* out, int cin, int cout, cudaStream_t s) {
-  if (cin == 16) return launch_cl<NPAD, 16>(m, feats, w, bias, out, cin, cout, s);
-  if (cin == 32) return launch_cl<NPAD, 32>(m, feats, w, bias, out, cin, cout, s);
-  return launch_cl<NPAD, 64>(m, feats, w, bias, out, cin, cout, s);
+cudaError_t launch_npad(const sc_map* m, const void* feats, const void* w, const Epilogue& ep,
+                        int cin, int cout, cudaStream_t s) {
+  if (cin == 16) return launch_cl<NPAD, 16>(m, feats, w, ep, cin, cout, s);
+  if (cin == 32) return launch_cl<NPAD, 32>(m, feats, w, ep, cin, cout, s);
+  return launch_cl<NPAD, 64>(m, feats, w, ep, cin, cout, s);
 }
 
 }  // namespace
@@ -829,15 +898,14 @@ bool conv_tc_supported(int cin, int cout) {
 }
 
 cudaError_t launch_conv_tc_bf16(const sc_map* m, const void* feats, const void* w,
-                                const float* bias, float* out, int cin, int cout,
-                                cudaStream_t s) {
+                                const Epilogue& ep, int cin, int cout, cudaStream_t s) {
   if (!conv_tc_supported(cin, cout)) return cudaErrorNotSupported;
   const int npad = (cout + 63) / 64 * 64;
   switch (npad) {
-    case 64: return launch_npad<64>(m, feats, w, bias, out, cin, cout, s);
-    case 128: return launch_npad<128>(m, feats, w, bias, out, cin, cout, s);
-    case 192: return launch_npad<192>(m, feats, w, bias, out, cin, cout, s);
-    default: return launch_npad<256>(m, feats, w, bias, out, cin, cout, s);
+    case 64: return launch_npad<64>(m, feats, w, ep, cin, cout, s);
+    case 128: return launch_npad<128>(m, feats, w, ep, cin, cout, s);
+    case 192: return launch_npad<192>(m, feats, w, ep, cin, cout, s);
+    default: return launch_npad<256>(m, feats, w, ep, cin, cout, s);
   }
 }
 

@@ -421,13 +421,29 @@ cudaError_t launch_nbr_to_row_major(const sc_map* m, int32_t* nbr_out, cudaStrea
 cudaError_t launch_pairs(const sc_map* m, int64_t* off_host, int32_t* in, int32_t* out,
                          void* scratch, cudaStream_t s);
 size_t pairs_scratch_bytes(int64_t n);
+// The convolution's fused epilogue ("Porting TRELLIS.2 From Python to Rust
+// and Metal", section V: bias, rounding, activation and the residual add in
+// the same pass): out = act(acc + bias) + residual, in fp32, then stored as
+// fp32 or rounded to bf16 (nearest, ties to even).
+struct Epilogue {
+  const float* bias;     // [cout] or nullptr
+  const void* residual;  // [n][cout] in the output dtype, or nullptr
+  void* out;             // [n][cout]
+  int act;               // SC_ACT_NONE / SC_ACT_RELU / SC_ACT_SILU
+  int out_bf16;          // 1: bf16 output, 0: fp32
+};
+
+__device__ __forceinline__ float apply_act(float v, int act) {
+  if (act == SC_ACT_RELU) return fmaxf(v, 0.f);
+  if (act == SC_ACT_SILU) return v / (1.f + __expf(-v));  // v * sigmoid(v); -> -0 as v -> -inf
+  return v;
+}
+
 cudaError_t launch_conv_simt_f32(const sc_map* m, const float* feats, const float* w,
-                                 const float* bias, float* out, int cin, int cout,
-                                 cudaStream_t s);
+                                 const Epilogue& ep, int cin, int cout, cudaStream_t s);
 // Returns cudaErrorNotSupported for shapes outside the tensor-core envelope.
 cudaError_t launch_conv_tc_bf16(const sc_map* m, const void* feats, const void* w,
-                                const float* bias, float* out, int cin, int cout,
-                                cudaStream_t s);
+                                const Epilogue& ep, int cin, int cout, cudaStream_t s);
 bool conv_tc_supported(int cin, int cout);
 // Process-wide count of the kernels this library has launched (host side).
 void note_launches(int k);

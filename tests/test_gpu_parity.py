@@ -339,3 +339,114 @@ def test_forward_rejects_bad_arguments(sc):
     assert lib.sc_forward(P(m.ptr), None, P(w.data_ptr()), None,
                           P(out.data_ptr()), 64, 64, 1, None) == sc.SC_ERR_INVALID_ARG
     m.free()
+
+
+# ---------------------------------------------------------------------------
+# fused epilogue: out = act(conv + bias) + residual, rounded once to the
+# output dtype ("Porting TRELLIS.2 From Python to Rust and Metal", section V)
+
+_ORACLE_CONV = {}
+
+
+def _oracle_conv_full(key):
+    if key not in _ORACLE_CONV:
+        p = synth.make_problem(key)
+        _ORACLE_CONV[key] = oracle.sparse_conv(p.coords, p.res, p.feats, p.weight, p.bias)
+    return _ORACLE_CONV[key]
+
+
+def bf16_ulp(x):
+    """Spacing of bf16 values at |x| (2^-133 below fp32's normal range)."""
+    _, e = np.frexp(np.abs(x))
+    return np.ldexp(1.0, np.maximum(e, -125) - 8)
+
+
+def check_epilogue_out(got, ref, odt, in_dtype, what):
+    """fp32 output: the convolution's bars.  bf16 output: within one bf16
+    spacing of the oracle's value rounded to bf16 (the GPU rounds its fp32
+    result, which can sit on the other side of a rounding boundary), plus the
+    fp32 accumulation error, and equal to it for nearly every element."""
+    if odt == "f32":
+        assert_close(got, ref, in_dtype, what)
+        return
+    rref = oracle.round_bf16(ref)
+    rms = np.linalg.norm(ref) / np.sqrt(ref.size)
+    err = np.abs(got - rref)
+    bound = bf16_ulp(ref) + 1e-4 * rms
+    assert np.all(err <= bound), "%s: %d elements beyond one bf16 spacing" % (
+        what, int((err > bound).sum()))
+    frac = np.mean(got == rref)
+    assert frac >= 0.95, "%s: only %.3f of elements equal the rounded oracle" % (what, frac)
+
+
+def _residual(n, cout, odt, seed):
+    r = np.random.default_rng(seed).standard_normal((n, cout)).astype(np.float32)
+    if odt == "bf16":
+        r = torch.from_numpy(r).to(torch.bfloat16).to(torch.float32).numpy()
+    return r
+
+
+@pytest.mark.parametrize("key", [1, 2])
+@pytest.mark.parametrize("act", ["none", "relu", "silu"])
+@pytest.mark.parametrize("resid", [False, True])
+@pytest.mark.parametrize("odt", ["f32", "bf16"])
+def test_fused_epilogue(sc, key, act, resid, odt):
+    p = synth.make_problem(key)
+    cout = p.weight.shape[2]
+    tin = torch.bfloat16 if p.config.dtype == "bf16" else torch.float32
+    tout = torch.bfloat16 if odt == "bf16" else torch.float32
+    r = _residual(p.n, cout, odt, 100 + key) if resid else None
+    m, _ = gpu_map(sc, p.coords, p.res)
+    out = sc.sc_forward_ex(m, to_dev(p.feats, tin), to_dev(p.weight, tin), to_dev(p.bias),
+                           residual=None if r is None else to_dev(r, tout), act=act,
+                           out_dtype=tout)
+    sc.sc_device_status(m)
+    got = out.float().cpu().numpy().astype(np.float64)
+    m.free()
+    acts = {"none": oracle.ACT_NONE, "relu": oracle.ACT_RELU, "silu": oracle.ACT_SILU}
+    ref = oracle.epilogue(_oracle_conv_full(key), acts[act], r)
+    check_epilogue_out(got, ref, odt, p.config.dtype, "config %d %s resid=%s %s" % (
+        key, act, resid, odt))
+
+
+@pytest.mark.parametrize("act,odt", [("none", "f32"), ("silu", "bf16"), ("relu", "f32")])
+def test_fused_epilogue_split_shapes(sc, act, odt):
+    """64^3, C=256: with act none and fp32 output the last partial round of
+    tiles is split and its parts add the residual in the last part; an
+    activation or bf16 output runs unsplit."""
+    p = synth.make_problem(3)
+    cout = p.weight.shape[2]
+    tout = torch.bfloat16 if odt == "bf16" else torch.float32
+    r = _residual(p.n, cout, odt, 7)
+    m, nbr = gpu_map(sc, p.coords, p.res)
+    out = sc.sc_forward_ex(m, to_dev(p.feats, torch.bfloat16), to_dev(p.weight, torch.bfloat16),
+                           to_dev(p.bias), residual=to_dev(r, tout), act=act, out_dtype=tout)
+    sc.sc_device_status(m)
+    got = out.float().cpu().numpy().astype(np.float64)
+    m.free()
+    rng = np.random.default_rng(33)
+    rows = np.unique(np.concatenate([np.arange(0, 256), np.arange(p.n - 2000, p.n),
+                                     rng.choice(p.n, size=2000, replace=False)]))
+    acts = {"none": oracle.ACT_NONE, "relu": oracle.ACT_RELU, "silu": oracle.ACT_SILU}
+    ref = oracle.epilogue(oracle.conv(nbr[rows], p.feats, p.weight, p.bias), acts[act], r[rows])
+    check_epilogue_out(got[rows], ref, odt, "bf16", "split %s %s" % (act, odt))
+
+
+def test_forward_ex_rejects_bad_epilogue_arguments(sc):
+    import ctypes
+    p = synth.make_problem(1)
+    m, _ = gpu_map(sc, p.coords, p.res)
+    f = to_dev(p.feats)
+    w = to_dev(p.weight)
+    out = torch.empty((p.n, p.weight.shape[2]), device="cuda")
+    lib = sc.load_library()
+    P = ctypes.c_void_p
+    args = (P(m.ptr), P(f.data_ptr()), P(w.data_ptr()), None, None, P(out.data_ptr()),
+            f.shape[1], out.shape[1], sc.SC_F32)
+    assert lib.sc_forward_ex(*args, 7, sc.SC_F32, None) == sc.SC_ERR_INVALID_ARG
+    assert lib.sc_forward_ex(*args, sc.SC_ACT_RELU, 5, None) == sc.SC_ERR_INVALID_ARG
+    misaligned = P(out.data_ptr() + 4)
+    assert lib.sc_forward_ex(P(m.ptr), P(f.data_ptr()), P(w.data_ptr()), None, misaligned,
+                             P(out.data_ptr()), f.shape[1], out.shape[1], sc.SC_F32,
+                             sc.SC_ACT_NONE, sc.SC_F32, None) == sc.SC_ERR_INVALID_ARG
+    m.free()

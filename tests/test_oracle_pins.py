@@ -312,3 +312,119 @@ def test_planted_mistakes_are_caught(name, tmp_path):
         except (AssertionError, oracle.OracleError, IndexError):
             failed.append(check.__name__)
     assert failed, "no pin caught the planted mistake %s" % name
+
+
+# ----------------------------------------------------------------------------
+# the fused epilogue ("Porting TRELLIS.2 From Python to Rust and Metal",
+# section V): out = act(conv + bias) + residual, rounded once to the output
+# type.  Pinned by closed forms, identities of the activations, the rounding
+# rule's worked cases, and an independent bf16 conversion (torch's).
+
+def check_activation(act_fn):
+    x = np.array([-3.0, -0.5, 0.0, 0.25, 7.0])
+    np.testing.assert_array_equal(act_fn(x, oracle.ACT_NONE), x)
+    np.testing.assert_array_equal(act_fn(x, oracle.ACT_RELU), [0.0, 0.0, 0.0, 0.25, 7.0])
+    s = lambda v: act_fn(np.asarray(v, np.float64), oracle.ACT_SILU)
+    # sigmoid(ln 3) = 3/4, sigmoid(-ln 3) = 1/4
+    np.testing.assert_allclose(s([np.log(3.0), -np.log(3.0)]),
+                               [0.75 * np.log(3.0), -0.25 * np.log(3.0)], rtol=1e-15)
+    # silu(x) - silu(-x) = x (sigmoid(x) + sigmoid(-x) = 1), silu(0) = 0
+    xs = np.linspace(-40.0, 40.0, 161)
+    np.testing.assert_allclose(s(xs) - s(-xs), xs, rtol=1e-14, atol=1e-14)
+    assert s([0.0])[0] == 0.0
+    # limits, with no overflow at large |x|: silu(x) -> x and -> 0
+    big = s([800.0, -800.0])
+    assert big[0] == 800.0 and big[1] == 0.0
+
+
+def check_epilogue(epi_fn):
+    v = np.array([[-1.0, 2.0, -0.5]])
+    r = np.array([[2.0, -1.0, 0.5]])
+    # the residual is added after the activation
+    np.testing.assert_array_equal(epi_fn(v, oracle.ACT_RELU, r), [[2.0, 1.0, 0.5]])
+    np.testing.assert_array_equal(epi_fn(v, oracle.ACT_NONE, r), v + r)
+    np.testing.assert_array_equal(epi_fn(v, oracle.ACT_RELU, None), [[0.0, 2.0, 0.0]])
+
+
+def check_round_bf16(rnd):
+    u = 2.0 ** -7  # bf16 spacing in [1, 2)
+    cases = {
+        1.0 + u / 2: 1.0,                 # tie -> even (mantissa ...0)
+        1.0 + 3 * u / 2: 1.0 + 2 * u,     # tie -> even (mantissa ...10)
+        1.0 + u / 2 + 2.0 ** -30: 1.0 + u,  # above the tie
+        1.0 + u / 2 - 2.0 ** -30: 1.0,    # below the tie
+        -(1.0 + 3 * u / 2): -(1.0 + 2 * u),
+        3.0: 3.0,
+        1.0 / 3.0: float.fromhex("0x1.560p-2"),  # 0.0101010101 -> 8 significant bits
+        2.0 ** -130 * 1.3: 10 * 2.0 ** -133,     # below 2^-126 the spacing is 2^-133
+        float.fromhex("0x1.ffp127"): np.inf,     # tie past the largest finite -> inf
+        0.0: 0.0,
+    }
+    got = rnd(np.array(list(cases.keys())))
+    np.testing.assert_array_equal(got, np.array(list(cases.values())))
+
+
+def check_round_bf16_against_torch(rnd):
+    # fp32-representable values: rounding them directly to bf16 and torch's
+    # fp32 -> bf16 conversion (an independent implementation) must agree
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal(20000) * np.exp(rng.uniform(-30, 30, 20000))).astype(np.float32)
+    x = np.concatenate([x, np.float32([1.00390625, 1.01171875, -2.0078125, 65504.0])])
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(rnd(x.astype(np.float64)), want)
+
+
+EPILOGUE_CHECKS = [
+    lambda a, e, r: check_activation(a),
+    lambda a, e, r: check_epilogue(e),
+    lambda a, e, r: check_round_bf16(r),
+    lambda a, e, r: check_round_bf16_against_torch(r),
+]
+
+
+def test_epilogue_pins():
+    for chk in EPILOGUE_CHECKS:
+        chk(oracle.activation, oracle.epilogue, oracle.round_bf16)
+
+
+def _mutant_round(mode):
+    def rnd(v):
+        v = np.asarray(v, np.float64)
+        out = np.zeros_like(v)
+        nz = (v != 0.0) & np.isfinite(v)
+        _, e = np.frexp(v[nz])
+        step = np.ldexp(1.0, np.maximum(e, -125) - 8)
+        t = v[nz] / step
+        q = np.trunc(t) if mode == "truncate" else np.sign(t) * np.floor(np.abs(t) + 0.5)
+        out[nz] = q * step
+        out[~nz] = v[~nz]
+        return out
+    return rnd
+
+
+EPILOGUE_MUTANTS = {
+    "residual_before_activation": (
+        oracle.activation,
+        lambda v, act=0, residual=None: oracle.activation(
+            np.asarray(v, np.float64) + (0.0 if residual is None else residual), act),
+        oracle.round_bf16),
+    "silu_sign_slip": (
+        lambda v, act: (np.asarray(v, np.float64) / (1.0 + np.exp(np.asarray(v, np.float64)))
+                        if act == oracle.ACT_SILU else oracle.activation(v, act)),
+        oracle.epilogue, oracle.round_bf16),
+    "round_ties_away": (oracle.activation, oracle.epilogue, _mutant_round("away")),
+    "round_truncate": (oracle.activation, oracle.epilogue, _mutant_round("truncate")),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EPILOGUE_MUTANTS))
+def test_planted_epilogue_mistakes_are_caught(name):
+    fns = EPILOGUE_MUTANTS[name]
+    failed = 0
+    with np.errstate(over="ignore", invalid="ignore"):
+        for chk in EPILOGUE_CHECKS:
+            try:
+                chk(*fns)
+            except AssertionError:
+                failed += 1
+    assert failed, "no epilogue pin caught %s" % name
