@@ -587,7 +587,78 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + acc * NPAD;
       float* stg = s_epi + warp * (32 * kStageRow);
+      // Column-group q of a chunk: rows 4q + lane / 8, columns 4 (lane % 8)
+      // of the chunk's 32.  Residual values of half h (groups 4h .. 4h + 3).
+      auto load_resid = [&](int ch, int h, float4 (&rv)[4]) {
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          const int q = 4 * h + qq;
+          const int c = ch * 32 + 4 * (lane & 7);
+          const int64_t row = wrow0 + 4 * q + (lane >> 3);
+          rv[qq] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (resid && row < p.n && c < p.cout) {
+            const int64_t e = row * p.cout + c;
+            if (p.out_bf16) {
+              const uint2 rb = __ldg(reinterpret_cast<const uint2*>(
+                  static_cast<const __nv_bfloat16*>(p.residual) + e));
+              rv[qq].x = __uint_as_float(rb.x << 16);  // bf16 -> fp32 is exact: the high half
+              rv[qq].y = __uint_as_float(rb.x & 0xffff0000u);
+              rv[qq].z = __uint_as_float(rb.y << 16);
+              rv[qq].w = __uint_as_float(rb.y & 0xffff0000u);
+            } else {
+              rv[qq] = __ldg(
+                  reinterpret_cast<const float4*>(static_cast<const float*>(p.residual) + e));
+            }
+          }
+        }
+      };
+      // Half h of the chunk from the staging block out to global memory:
+      // activation, residual, rounding; each store covers four rows x 128
+      // contiguous bytes (64 for bf16).
+      auto store_half = [&](int ch, int h, const float4 (&rv)[4]) {
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          const int q = 4 * h + qq;
+          const int r = 4 * q + (lane >> 3), g = lane & 7;
+          const int c = ch * 32 + 4 * g;
+          const int64_t row = wrow0 + r;
+          float4 o = *reinterpret_cast<const float4*>(stg + r * kStageRow + 4 * g);
+          if (row < p.n && c < p.cout) {
+            const int64_t e = row * p.cout + c;
+            if (p.act) {
+              o.x = apply_act(o.x, p.act);
+              o.y = apply_act(o.y, p.act);
+              o.z = apply_act(o.z, p.act);
+              o.w = apply_act(o.w, p.act);
+            }
+            o.x += rv[qq].x;
+            o.y += rv[qq].y;
+            o.z += rv[qq].z;
+            o.w += rv[qq].w;
+            if (p.out_bf16) {
+              const __nv_bfloat162 b01 = __float22bfloat162_rn(make_float2(o.x, o.y));
+              const __nv_bfloat162 b23 = __float22bfloat162_rn(make_float2(o.z, o.w));
+              uint2 pk;
+              pk.x = *reinterpret_cast<const uint32_t*>(&b01);
+              pk.y = *reinterpret_cast<const uint32_t*>(&b23);
+              __stcs(reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + e), pk);
+            } else {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + e);
+              if (add)
+                atomicAdd(dst, o);
+              else
+                __stcs(dst, o);
+            }
+          }
+        }
+      };
       for (int ch = 0; ch < nchunks; ++ch) {
+        // Residual loads are issued early (the first half before the TMEM
+        // load, the second before the first half is stored), so their L2
+        // latency overlaps work; out and residual may alias, so no load can
+        // move past a store by itself.
+        float4 ra[4], rb[4];
+        load_resid(ch, 0, ra);
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + ch * 32, v);
         tmem_ld_wait();
@@ -603,72 +674,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           *reinterpret_cast<float4*>(stg + lane * kStageRow + 4 * q) = o;
         }
         __syncwarp();
-        // ... and out again by column groups: each store instruction writes
-        // four rows x 128 contiguous bytes (64 for bf16), after the rest of
-        // the epilogue (activation, residual, rounding).
-        // Two halves of four column groups; each half's residual values are
-        // loaded before any of its stores (out and residual may alias, so a
-        // load cannot move past a store).  Four, not eight, at a time: the
-        // kernel's 14 warps leave 128 registers a thread.
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float4 rv[4];
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            const int q = 4 * h + qq;
-            const int r = 4 * q + (lane >> 3), c = ch * 32 + 4 * (lane & 7);
-            const int64_t row = wrow0 + r;
-            rv[qq] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (resid && row < p.n && c < p.cout) {
-              const int64_t e = row * p.cout + c;
-              if (p.out_bf16) {
-                const uint2 rb = __ldg(reinterpret_cast<const uint2*>(
-                    static_cast<const __nv_bfloat16*>(p.residual) + e));
-                rv[qq].x = __uint_as_float(rb.x << 16);  // bf16 -> fp32 is exact: the high half
-                rv[qq].y = __uint_as_float(rb.x & 0xffff0000u);
-                rv[qq].z = __uint_as_float(rb.y << 16);
-                rv[qq].w = __uint_as_float(rb.y & 0xffff0000u);
-              } else {
-                rv[qq] = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.residual) + e));
-              }
-            }
-          }
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            const int q = 4 * h + qq;
-            const int r = 4 * q + (lane >> 3), g = lane & 7;
-            const int c = ch * 32 + 4 * g;
-            const int64_t row = wrow0 + r;
-            float4 o = *reinterpret_cast<const float4*>(stg + r * kStageRow + 4 * g);
-            if (row < p.n && c < p.cout) {
-              const int64_t e = row * p.cout + c;
-              if (p.act) {
-                o.x = apply_act(o.x, p.act);
-                o.y = apply_act(o.y, p.act);
-                o.z = apply_act(o.z, p.act);
-                o.w = apply_act(o.w, p.act);
-              }
-              o.x += rv[qq].x;
-              o.y += rv[qq].y;
-              o.z += rv[qq].z;
-              o.w += rv[qq].w;
-              if (p.out_bf16) {
-                const __nv_bfloat162 b01 = __float22bfloat162_rn(make_float2(o.x, o.y));
-                const __nv_bfloat162 b23 = __float22bfloat162_rn(make_float2(o.z, o.w));
-                uint2 pk;
-                pk.x = *reinterpret_cast<const uint32_t*>(&b01);
-                pk.y = *reinterpret_cast<const uint32_t*>(&b23);
-                __stcs(reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + e), pk);
-              } else {
-                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + e);
-                if (add)
-                  atomicAdd(dst, o);
-                else
-                  __stcs(dst, o);
-              }
-            }
-          }
-        }
+        // ... and out again by column groups.
+        load_resid(ch, 1, rb);
+        store_half(ch, 0, ra);
+        store_half(ch, 1, rb);
         __syncwarp();
       }
       tc_fence_before();

@@ -435,7 +435,9 @@ struct Epilogue {
 
 __device__ __forceinline__ float apply_act(float v, int act) {
   if (act == SC_ACT_RELU) return fmaxf(v, 0.f);
-  if (act == SC_ACT_SILU) return v / (1.f + __expf(-v));  // v * sigmoid(v); -> -0 as v -> -inf
+  // v * sigmoid(v) = v / (1 + e^-v), by the fast divide (2 ulp); as v -> -inf
+  // the denominator passes 2^126 and the quotient is -0, the function's limit.
+  if (act == SC_ACT_SILU) return __fdividef(v, 1.f + __expf(-v));
   return v;
 }
 
