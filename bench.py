@@ -153,7 +153,7 @@ def oracle_sample_run(p, rows, threads=0):
     return dt, pairs
 
 
-def cpu_baseline(p, target_s=12.0):
+def cpu_baseline(p, target_s=20.0):
     """The oracle as it stands on the host cores, for ~target_s seconds: the
     whole workload (map build + fp64 convolution of every row) repeated while
     it fits, else the map build and a row sample sized to the target."""
@@ -239,7 +239,7 @@ def run_reference(args):
 # valid only for the kernel source it was measured on (sha1 of the file).
 MEASURED_TRAFFIC = {
     # workload name: (sha1 of sc_conv_tc.cu, bytes per launch)
-    "sq3x64_30k_c256_bf16": ("736da9d2ee4ae7d605e3c01bc76456b2944740d2", 33268480 + 41728),
+    "sq3x64_30k_c256_bf16": ("59f8a28fa8e732fd5411a89ffff1be43c727a8c8", 33268736 + 58624),
 }
 
 

@@ -257,7 +257,9 @@ __global__ void __launch_bounds__(256) k_zero_rows(float4* __restrict__ p, int64
     p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-template <int NPAD, int CS, int CL>
+// FUSED: the epilogue applies an activation, adds a residual or rounds to
+// bf16 (the plain variant only adds the bias and stores fp32).
+template <int NPAD, int CS, int CL, bool FUSED>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_conv_tc(const __grid_constant__ CUtensorMap tm_b, const TcArgs p) {
   using C = TcCfg<NPAD, CS>;
@@ -566,7 +568,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool add = wi.part >= 0;
       const bool last = !add || wi.part == p.split - 1;
       const float bscale = last ? 1.f : 0.f;
-      const bool resid = p.residual != nullptr && last;
+      const bool resid = FUSED && p.residual != nullptr && last;
       const int64_t wrow0 = (wi.unit * CL + rank) * kTileRows + warp * 32;  // this warp's rows
       if (resid && wrow0 + lane < p.n) {
         // This thread's row of the residual into L2 while the main loop runs
@@ -658,7 +660,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // latency overlaps work; out and residual may alias, so no load can
         // move past a store by itself.
         float4 ra[4], rb[4];
-        load_resid(ch, 0, ra);
+        if constexpr (FUSED) load_resid(ch, 0, ra);
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + ch * 32, v);
         tmem_ld_wait();
@@ -675,9 +677,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
         // ... and out again by column groups.
-        load_resid(ch, 1, rb);
-        store_half(ch, 0, ra);
-        store_half(ch, 1, rb);
+        if constexpr (FUSED) {
+          load_resid(ch, 1, rb);
+          store_half(ch, 0, ra);
+          store_half(ch, 1, rb);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int r = 4 * q + (lane >> 3), g = lane & 7;
+            const int c = ch * 32 + 4 * g;
+            const int64_t row = wrow0 + r;
+            const float4 o = *reinterpret_cast<const float4*>(stg + r * kStageRow + 4 * g);
+            if (row < p.n && c < p.cout) {
+              float4* dst =
+                  reinterpret_cast<float4*>(static_cast<float*>(p.out) + row * p.cout + c);
+              if (add)
+                atomicAdd(dst, o);
+              else
+                __stcs(dst, o);
+            }
+          }
+        }
         __syncwarp();
       }
       tc_fence_before();
@@ -788,11 +808,11 @@ int tail_split(int64_t nunits, int64_t G, int max_stages) {
   return best_t < 0.95 * t1 ? best : 1;
 }
 
-template <int NPAD, int CS, int CL>
+template <int NPAD, int CS, int CL, bool FUSED>
 cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, const Epilogue& ep,
                          int cin, int cout, cudaStream_t s) {
   using C = TcCfg<NPAD, CS>;
-  auto kern = k_conv_tc<NPAD, CS, CL>;
+  auto kern = k_conv_tc<NPAD, CS, CL, FUSED>;
   static LaunchCache cache;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -884,8 +904,12 @@ cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, cons
 template <int NPAD, int CS>
 cudaError_t launch_cl(const sc_map* m, const void* feats, const void* w, const Epilogue& ep,
                       int cin, int cout, cudaStream_t s) {
-  if (cluster_size(NPAD) == 2) return launch_typed<NPAD, CS, 2>(m, feats, w, ep, cin, cout, s);
-  return launch_typed<NPAD, CS, 1>(m, feats, w, ep, cin, cout, s);
+  const bool fused = ep.act || ep.residual || ep.out_bf16;
+  if (cluster_size(NPAD) == 2)
+    return fused ? launch_typed<NPAD, CS, 2, true>(m, feats, w, ep, cin, cout, s)
+                 : launch_typed<NPAD, CS, 2, false>(m, feats, w, ep, cin, cout, s);
+  return fused ? launch_typed<NPAD, CS, 1, true>(m, feats, w, ep, cin, cout, s)
+               : launch_typed<NPAD, CS, 1, false>(m, feats, w, ep, cin, cout, s);
 }
 
 template <int NPAD>
