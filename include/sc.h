@@ -62,7 +62,7 @@ typedef enum {
   SC_ERR_DEVICE_TIMEOUT = 9 /* a bounded device wait ran out (see sc_device_status) */
 } sc_status;
 
-typedef enum { SC_F32 = 0, SC_BF16 = 1 } sc_dtype;
+typedef enum { SC_F32 = 0, SC_BF16 = 1, SC_F16 = 2 } sc_dtype;
 
 /* Activation of the fused epilogue (sc_forward_ex). */
 typedef enum {
@@ -119,9 +119,9 @@ SC_API sc_handle sc_build_map(const int32_t* coords, int64_t n, int32_t res, voi
  *   weight  device [27][cin][cout], dtype `dtype`, row-major, 16-byte aligned.
  *   bias    device fp32 [cout], or NULL for zero bias.
  *   out     device fp32 [n][cout], row-major, 16-byte aligned; fully written.
- *   dtype   SC_BF16: tensor-core path (tcgen05, bf16 x bf16 -> fp32 in TMEM);
- *           cin in {16, 32} or a multiple of 64 up to 1024; cout a multiple of
- *           16 up to 256.
+ *   dtype   SC_BF16 / SC_F16: tensor-core path (tcgen05, bf16 x bf16 or
+ *           fp16 x fp16 -> fp32 in TMEM); cin in {16, 32} or a multiple of
+ *           64 up to 1024; cout a multiple of 16 up to 256.
  *           SC_F32: fp32 FFMA path (no reduced-precision products); any
  *           cin >= 1 and 1 <= cout <= 256.
  * Asynchronous on `stream`; never synchronises.  Returns SC_ERR_UNSUPPORTED
@@ -143,9 +143,11 @@ SC_API sc_status sc_forward(sc_handle h, const void* feats, const void* weight, 
  *   residual  device [n][cout] in out_dtype, 16-byte aligned, or NULL.
  *   out       device [n][cout] in out_dtype, 16-byte aligned; fully written.
  *   act       SC_ACT_NONE, SC_ACT_RELU or SC_ACT_SILU.
- *   out_dtype SC_F32 or SC_BF16 (either with either input dtype).
+ *   out_dtype SC_F32, SC_BF16 or SC_F16 (any with any input dtype); bf16
+ *             and fp16 by rounding to nearest, ties to even (fp16 overflows
+ *             to infinity past 65,504).
  * sc_forward(...) is sc_forward_ex(..., NULL residual, SC_ACT_NONE, SC_F32).
- * On the SC_BF16 path an activation or a bf16 output turns the tail split
+ * On the tensor-core path an activation or a 16-bit output turns the tail split
  * (see sc_forward) off, since neither can be applied to a partial sum; a
  * residual alone keeps it (the last part adds it).
  * Errors as sc_forward, plus SC_ERR_INVALID_ARG for a bad act or out_dtype.

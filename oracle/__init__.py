@@ -184,22 +184,34 @@ def epilogue(conv_out, act=ACT_NONE, residual=None):
     return y
 
 
-def round_bf16(v):
-    """Round fp64 values to bfloat16 (8 significant bits, fp32's exponent
-    range), nearest with ties to even; returned as fp64.  Written from the
-    format's definition: v = m * 2^e with 0.5 <= |m| < 1 keeps m to 8 bits,
-    i.e. v is rounded to a multiple of 2^(e - 8); below fp32's normal range
-    (2^-126) the spacing stays 2^-133.  Values past the largest finite bf16
-    become infinities."""
+def _round_to_format(v, sig_bits, e_min, max_finite):
+    """Round fp64 values to a binary format with `sig_bits` significant bits,
+    nearest with ties to even: v = m * 2^e with 0.5 <= |m| < 1 keeps m to
+    sig_bits bits, i.e. v becomes a multiple of 2^(e - sig_bits); below the
+    format's smallest normal (e < e_min) the spacing stays 2^(e_min -
+    sig_bits).  Results past max_finite become infinities."""
     v = np.asarray(v, dtype=np.float64)
     out = np.zeros_like(v)
     nz = (v != 0.0) & np.isfinite(v)
     _, e = np.frexp(v[nz])
-    e = np.maximum(e, -125)
-    step = np.ldexp(1.0, e - 8)
+    step = np.ldexp(1.0, np.maximum(e, e_min) - sig_bits)
     q = np.rint(v[nz] / step) * step  # rint: round half to even
-    big = np.abs(q) > float.fromhex("0x1.fep127")
+    big = np.abs(q) > max_finite
     q[big] = np.copysign(np.inf, q[big])
     out[nz] = q
     out[~nz] = v[~nz]
     return out
+
+
+def round_bf16(v):
+    """Round fp64 values to bfloat16 (8 significant bits, fp32's exponent
+    range: smallest normal 2^-126, so the spacing below it is 2^-133; largest
+    finite 0x1.fep127), nearest with ties to even; returned as fp64."""
+    return _round_to_format(v, 8, -125, float.fromhex("0x1.fep127"))
+
+
+def round_f16(v):
+    """Round fp64 values to IEEE binary16 (11 significant bits, smallest
+    normal 2^-14 so subnormal spacing 2^-24, largest finite 65504), nearest
+    with ties to even; returned as fp64."""
+    return _round_to_format(v, 11, -13, 65504.0)

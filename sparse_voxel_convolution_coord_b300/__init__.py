@@ -23,7 +23,7 @@ __all__ = [
     "sc_get_neighbor_table", "sc_get_pairs", "sc_device_status", "sc_last_error",
     "sc_last_error_msg", "sc_version", "sc_set_deterministic", "sc_kernel_launches", "SC_OK", "SC_ERR_INVALID_ARG", "SC_ERR_COORD_RANGE",
     "SC_ERR_DUPLICATE", "SC_ERR_TABLE_FULL", "SC_ERR_UNSUPPORTED", "SC_ERR_ALLOC",
-    "SC_ERR_CUDA", "SC_ERR_BAD_HANDLE", "SC_ERR_DEVICE_TIMEOUT", "SC_F32", "SC_BF16",
+    "SC_ERR_CUDA", "SC_ERR_BAD_HANDLE", "SC_ERR_DEVICE_TIMEOUT", "SC_F32", "SC_BF16", "SC_F16",
     "SC_ACT_NONE", "SC_ACT_RELU", "SC_ACT_SILU", "sc_forward_ex",
 ]
 
@@ -34,7 +34,7 @@ HEADER = os.path.join(_ROOT, "include", "sc.h")
 (SC_OK, SC_ERR_INVALID_ARG, SC_ERR_COORD_RANGE, SC_ERR_DUPLICATE, SC_ERR_TABLE_FULL,
  SC_ERR_UNSUPPORTED, SC_ERR_ALLOC, SC_ERR_CUDA, SC_ERR_BAD_HANDLE,
  SC_ERR_DEVICE_TIMEOUT) = range(10)
-SC_F32, SC_BF16 = 0, 1
+SC_F32, SC_BF16, SC_F16 = 0, 1, 2
 SC_ACT_NONE, SC_ACT_RELU, SC_ACT_SILU = 0, 1, 2
 _ACTS = {"none": SC_ACT_NONE, "relu": SC_ACT_RELU, "silu": SC_ACT_SILU}
 
@@ -206,21 +206,25 @@ def sc_map_pairs(m: Map) -> int:
     return int(v)
 
 
+def _operand_dtype(feats):
+    import torch
+    codes = {torch.bfloat16: SC_BF16, torch.float16: SC_F16, torch.float32: SC_F32}
+    if feats.dtype not in codes:
+        raise ValueError("dtype must be bfloat16, float16 or float32")
+    return codes[feats.dtype]
+
+
 def sc_forward(m: Map, feats, weight, bias=None, out=None, stream=None):
     """out[N,cout] fp32 = bias + sum_k gather(feats, nbr[:,k]) @ weight[k].
 
-    feats [N,cin] and weight [27,cin,cout] are both bf16 (tensor-core path) or
-    both fp32 (FFMA path); bias fp32 [cout] or None.  Asynchronous.
+    feats [N,cin] and weight [27,cin,cout] are both bf16 or both fp16
+    (tensor-core path), or both fp32 (FFMA path); bias fp32 [cout] or None.
+    Asynchronous.
     """
     import torch
     if feats.dtype != weight.dtype:
         raise ValueError("feats and weight must have the same dtype")
-    if feats.dtype == torch.bfloat16:
-        dt = SC_BF16
-    elif feats.dtype == torch.float32:
-        dt = SC_F32
-    else:
-        raise ValueError("dtype must be bfloat16 or float32")
+    dt = _operand_dtype(feats)
     n, cin = feats.shape
     if weight.dim() != 3 or weight.shape[0] != 27 or weight.shape[1] != cin:
         raise ValueError("weight must be [27, cin, cout]")
@@ -242,24 +246,21 @@ def sc_forward_ex(m: Map, feats, weight, bias=None, residual=None, act="none",
                   out_dtype=None, out=None, stream=None):
     """Convolution with the fused epilogue: out = act(conv + bias) + residual.
 
-    act is "none", "relu" or "silu"; out_dtype torch.float32 (default) or
-    torch.bfloat16; residual [N,cout] in out_dtype or None.  Asynchronous.
+    act is "none", "relu" or "silu"; out_dtype torch.float32 (default),
+    torch.bfloat16 or torch.float16; residual [N,cout] in out_dtype or None.
+    Asynchronous.
     """
     import torch
     if feats.dtype != weight.dtype:
         raise ValueError("feats and weight must have the same dtype")
-    if feats.dtype == torch.bfloat16:
-        dt = SC_BF16
-    elif feats.dtype == torch.float32:
-        dt = SC_F32
-    else:
-        raise ValueError("dtype must be bfloat16 or float32")
+    dt = _operand_dtype(feats)
     if act not in _ACTS:
         raise ValueError("act must be one of %s" % sorted(_ACTS))
     out_dtype = torch.float32 if out_dtype is None else out_dtype
-    if out_dtype not in (torch.float32, torch.bfloat16):
-        raise ValueError("out_dtype must be float32 or bfloat16")
-    odt = SC_BF16 if out_dtype == torch.bfloat16 else SC_F32
+    odts = {torch.float32: SC_F32, torch.bfloat16: SC_BF16, torch.float16: SC_F16}
+    if out_dtype not in odts:
+        raise ValueError("out_dtype must be float32, bfloat16 or float16")
+    odt = odts[out_dtype]
     n, cin = feats.shape
     if weight.dim() != 3 or weight.shape[0] != 27 or weight.shape[1] != cin:
         raise ValueError("weight must be [27, cin, cout]")

@@ -366,16 +366,16 @@ sc_status sc_forward_ex(sc_handle h, const void* feats, const void* weight, cons
                         sc_dtype dtype, sc_activation act, sc_dtype out_dtype, void* stream) {
   if (!is_live(h)) return fail(SC_ERR_BAD_HANDLE, "sc_forward: handle is not live");
   if (cin < 1 || cout < 1) return fail(SC_ERR_INVALID_ARG, "sc_forward: cin/cout must be >= 1");
-  if (dtype != SC_F32 && dtype != SC_BF16)
+  if (dtype != SC_F32 && dtype != SC_BF16 && dtype != SC_F16)
     return fail(SC_ERR_UNSUPPORTED, "sc_forward: dtype %d not supported", (int)dtype);
-  if (out_dtype != SC_F32 && out_dtype != SC_BF16)
+  if (out_dtype != SC_F32 && out_dtype != SC_BF16 && out_dtype != SC_F16)
     return fail(SC_ERR_INVALID_ARG, "sc_forward_ex: out_dtype %d not supported", (int)out_dtype);
   if (act != SC_ACT_NONE && act != SC_ACT_RELU && act != SC_ACT_SILU)
     return fail(SC_ERR_INVALID_ARG, "sc_forward_ex: activation %d not supported", (int)act);
-  if (dtype == SC_BF16 && !sc::conv_tc_supported(cin, cout))
+  if (dtype != SC_F32 && !sc::conv_tc_supported(cin, cout))
     return fail(SC_ERR_UNSUPPORTED,
-                "sc_forward: bf16 needs cin in {16,32} or a multiple of 64 <= 1024 and cout a "
-                "multiple of 16 <= 256 (got cin=%d cout=%d)",
+                "sc_forward: bf16/fp16 need cin in {16,32} or a multiple of 64 <= 1024 and cout "
+                "a multiple of 16 <= 256 (got cin=%d cout=%d)",
                 cin, cout);
   if (dtype == SC_F32 && cout > 256)
     return fail(SC_ERR_UNSUPPORTED, "sc_forward: fp32 path supports cout <= 256 (got %d)", cout);
@@ -397,10 +397,10 @@ sc_status sc_forward_ex(sc_handle h, const void* feats, const void* weight, cons
   ep.residual = residual;
   ep.out = out;
   ep.act = (int)act;
-  ep.out_bf16 = out_dtype == SC_BF16 ? 1 : 0;
+  ep.out_half = out_dtype == SC_BF16 ? sc::kOutBf16 : (out_dtype == SC_F16 ? sc::kOutF16 : 0);
   cudaError_t e;
-  if (dtype == SC_BF16)
-    e = sc::launch_conv_tc_bf16(h, feats, weight, ep, cin, cout, s);
+  if (dtype != SC_F32)
+    e = sc::launch_conv_tc(h, feats, weight, dtype == SC_F16, ep, cin, cout, s);
   else
     e = sc::launch_conv_simt_f32(h, static_cast<const float*>(feats),
                                  static_cast<const float*>(weight), ep, cin, cout, s);

@@ -12,9 +12,10 @@
 // then, for each offset present in any of the block's rows, the W[k] slice
 // (32 rows x cout) is staged in shared memory by cp.async, double-buffered one
 // offset ahead, and shared by the 8 warps.  Each output row is written once,
-// no atomics, through the fused epilogue (activation, residual, fp32 or bf16
-// output).
+// no atomics, through the fused epilogue (activation, residual, fp32, bf16 or
+// fp16 output).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "sc_internal.cuh"
 
@@ -119,10 +120,13 @@ __global__ void __launch_bounds__(kSimtWarps * 32) k_conv_simt_f32(
       if (c >= cout) continue;
       const int64_t e = o * cout + c;
       float v = apply_act(acc[j] + (ep.bias ? __ldg(ep.bias + c) : 0.f), ep.act);
-      if (ep.out_bf16) {
+      if (ep.out_half == kOutBf16) {
         if (ep.residual)
           v += __bfloat162float(static_cast<const __nv_bfloat16*>(ep.residual)[e]);
         static_cast<__nv_bfloat16*>(ep.out)[e] = __float2bfloat16_rn(v);
+      } else if (ep.out_half == kOutF16) {
+        if (ep.residual) v += __half2float(static_cast<const __half*>(ep.residual)[e]);
+        static_cast<__half*>(ep.out)[e] = __float2half_rn(v);
       } else {
         if (ep.residual) v += __ldg(static_cast<const float*>(ep.residual) + e);
         static_cast<float*>(ep.out)[e] = v;

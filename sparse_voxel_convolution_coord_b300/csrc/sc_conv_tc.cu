@@ -67,6 +67,7 @@
 #include <cstring>
 #include <mutex>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
 #include "sc_internal.cuh"
@@ -121,7 +122,6 @@ struct TcCfg {
   static constexpr uint32_t kTmemCols = (2 * NPAD <= 128) ? 128 : (2 * NPAD <= 256 ? 256 : 512);
   static constexpr uint32_t kLayoutA = CS == 64 ? 2u : (CS == 32 ? 4u : 6u);
   static constexpr uint32_t kSboA = 8 * kRowBytes;
-  static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileRows, NPAD);
   static_assert(kStages >= 2, "pipeline needs two stages");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
 };
@@ -134,7 +134,8 @@ struct TcArgs {
   const void* residual;  // [n][cout] in the output dtype, or nullptr
   void* out;             // fp32 or bf16 [n][cout]
   int act;               // fused activation (SC_ACT_*)
-  int out_bf16;          // bf16 output (round to nearest even)
+  int out_half;          // 16-bit output (kOutBf16 / kOutF16, nearest even), 0: fp32
+  uint32_t idesc;        // MMA instruction descriptor (bf16 or fp16 operands)
   uint32_t* status;
   int64_t n;
   int64_t ntiles;
@@ -525,7 +526,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const uint64_t ad =
                   smem_desc(a_base + j * C::kASeg + kk * 32, 16, C::kSboA, C::kLayoutA);
               const uint64_t bd = smem_desc(b_base + (j * CS + kk * 16) * 128, 64 * 128, 1024, 2u);
-              tc_mma_bf16(d_tmem, ad, bd, C::kIdesc, (s | j | kk) != 0 ? 1u : 0u);
+              tc_mma_bf16(d_tmem, ad, bd, p.idesc, (s | j | kk) != 0 ? 1u : 0u);
             }
           }
           if constexpr (CL > 1)
@@ -573,7 +574,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (resid && wrow0 + lane < p.n) {
         // This thread's row of the residual into L2 while the main loop runs
         // (128-byte lines); the column-group loads below then hit L2.
-        const int rbytes = p.cout * (p.out_bf16 ? 2 : 4);
+        const int rbytes = p.cout * (p.out_half ? 2 : 4);
         const char* rrow = static_cast<const char*>(p.residual) + (wrow0 + lane) * rbytes;
         for (int off = 0; off < rbytes; off += 128)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(rrow + off));
@@ -600,13 +601,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           rv[qq] = make_float4(0.f, 0.f, 0.f, 0.f);
           if (resid && row < p.n && c < p.cout) {
             const int64_t e = row * p.cout + c;
-            if (p.out_bf16) {
+            if (p.out_half) {
               const uint2 rb = __ldg(reinterpret_cast<const uint2*>(
                   static_cast<const __nv_bfloat16*>(p.residual) + e));
-              rv[qq].x = __uint_as_float(rb.x << 16);  // bf16 -> fp32 is exact: the high half
-              rv[qq].y = __uint_as_float(rb.x & 0xffff0000u);
-              rv[qq].z = __uint_as_float(rb.y << 16);
-              rv[qq].w = __uint_as_float(rb.y & 0xffff0000u);
+              if (p.out_half == kOutBf16) {
+                rv[qq].x = __uint_as_float(rb.x << 16);  // bf16 -> fp32 is exact: the high half
+                rv[qq].y = __uint_as_float(rb.x & 0xffff0000u);
+                rv[qq].z = __uint_as_float(rb.y << 16);
+                rv[qq].w = __uint_as_float(rb.y & 0xffff0000u);
+              } else {
+                const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&rb.x));
+                const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&rb.y));
+                rv[qq] = make_float4(f01.x, f01.y, f23.x, f23.y);
+              }
             } else {
               rv[qq] = __ldg(
                   reinterpret_cast<const float4*>(static_cast<const float*>(p.residual) + e));
@@ -637,12 +644,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             o.y += rv[qq].y;
             o.z += rv[qq].z;
             o.w += rv[qq].w;
-            if (p.out_bf16) {
-              const __nv_bfloat162 b01 = __float22bfloat162_rn(make_float2(o.x, o.y));
-              const __nv_bfloat162 b23 = __float22bfloat162_rn(make_float2(o.z, o.w));
+            if (p.out_half) {
               uint2 pk;
-              pk.x = *reinterpret_cast<const uint32_t*>(&b01);
-              pk.y = *reinterpret_cast<const uint32_t*>(&b23);
+              if (p.out_half == kOutBf16) {
+                const __nv_bfloat162 b01 = __float22bfloat162_rn(make_float2(o.x, o.y));
+                const __nv_bfloat162 b23 = __float22bfloat162_rn(make_float2(o.z, o.w));
+                pk.x = *reinterpret_cast<const uint32_t*>(&b01);
+                pk.y = *reinterpret_cast<const uint32_t*>(&b23);
+              } else {
+                const __half2 h01 = __float22half2_rn(make_float2(o.x, o.y));
+                const __half2 h23 = __float22half2_rn(make_float2(o.z, o.w));
+                pk.x = *reinterpret_cast<const uint32_t*>(&h01);
+                pk.y = *reinterpret_cast<const uint32_t*>(&h23);
+              }
               __stcs(reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + e), pk);
             } else {
               float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + e);
@@ -740,14 +754,14 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-               CUtensorMapSwizzle swz) {
+               CUtensorMapSwizzle swz, CUtensorMapDataType dt) {
   auto fn = get_encode();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -809,8 +823,8 @@ int tail_split(int64_t nunits, int64_t G, int max_stages) {
 }
 
 template <int NPAD, int CS, int CL, bool FUSED>
-cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, const Epilogue& ep,
-                         int cin, int cout, cudaStream_t s) {
+cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, bool f16,
+                         const Epilogue& ep, int cin, int cout, cudaStream_t s) {
   using C = TcCfg<NPAD, CS>;
   auto kern = k_conv_tc<NPAD, CS, CL, FUSED>;
   static LaunchCache cache;
@@ -855,7 +869,8 @@ cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, cons
 
   alignas(64) CUtensorMap tm_b;
   if (!encode_2d(&tm_b, w, (uint64_t)cout, (uint64_t)kTaps * cin, (uint64_t)cout * 2, 64, CS,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
+                 CU_TENSOR_MAP_SWIZZLE_128B,
+                 f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
     return cudaErrorInvalidValue;
   TcArgs a;
   a.feats = static_cast<const __nv_bfloat16*>(feats);
@@ -865,7 +880,8 @@ cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, cons
   a.residual = ep.residual;
   a.out = ep.out;
   a.act = ep.act;
-  a.out_bf16 = ep.out_bf16;
+  a.out_half = ep.out_half;
+  a.idesc = idesc_bf16_f32(kTileRows, NPAD, f16);
   a.status = m->d_status;
   a.n = m->n;
   a.ntiles = m->ntiles;
@@ -875,7 +891,7 @@ cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, cons
   if (nunits == 0) return cudaSuccess;
   const int max_stages = CS == 64 ? kTaps * (cin / 64) : (kTaps + 64 / CS - 1) / (64 / CS);
   // An activation or a bf16 output cannot be applied to partial sums.
-  const int split = (ep.act || ep.out_bf16) ? 1 : tail_split(nunits, max_clusters, max_stages);
+  const int split = (ep.act || ep.out_half) ? 1 : tail_split(nunits, max_clusters, max_stages);
   a.split = split;
   a.tail = split > 1 ? (nunits >= max_clusters ? nunits % max_clusters : nunits) : 0;
   a.whole = nunits - a.tail;
@@ -902,22 +918,22 @@ cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, cons
 }
 
 template <int NPAD, int CS>
-cudaError_t launch_cl(const sc_map* m, const void* feats, const void* w, const Epilogue& ep,
-                      int cin, int cout, cudaStream_t s) {
-  const bool fused = ep.act || ep.residual || ep.out_bf16;
+cudaError_t launch_cl(const sc_map* m, const void* feats, const void* w, bool f16,
+                      const Epilogue& ep, int cin, int cout, cudaStream_t s) {
+  const bool fused = ep.act || ep.residual || ep.out_half;
   if (cluster_size(NPAD) == 2)
-    return fused ? launch_typed<NPAD, CS, 2, true>(m, feats, w, ep, cin, cout, s)
-                 : launch_typed<NPAD, CS, 2, false>(m, feats, w, ep, cin, cout, s);
-  return fused ? launch_typed<NPAD, CS, 1, true>(m, feats, w, ep, cin, cout, s)
-               : launch_typed<NPAD, CS, 1, false>(m, feats, w, ep, cin, cout, s);
+    return fused ? launch_typed<NPAD, CS, 2, true>(m, feats, w, f16, ep, cin, cout, s)
+                 : launch_typed<NPAD, CS, 2, false>(m, feats, w, f16, ep, cin, cout, s);
+  return fused ? launch_typed<NPAD, CS, 1, true>(m, feats, w, f16, ep, cin, cout, s)
+               : launch_typed<NPAD, CS, 1, false>(m, feats, w, f16, ep, cin, cout, s);
 }
 
 template <int NPAD>
-cudaError_t launch_npad(const sc_map* m, const void* feats, const void* w, const Epilogue& ep,
-                        int cin, int cout, cudaStream_t s) {
-  if (cin == 16) return launch_cl<NPAD, 16>(m, feats, w, ep, cin, cout, s);
-  if (cin == 32) return launch_cl<NPAD, 32>(m, feats, w, ep, cin, cout, s);
-  return launch_cl<NPAD, 64>(m, feats, w, ep, cin, cout, s);
+cudaError_t launch_npad(const sc_map* m, const void* feats, const void* w, bool f16,
+                        const Epilogue& ep, int cin, int cout, cudaStream_t s) {
+  if (cin == 16) return launch_cl<NPAD, 16>(m, feats, w, f16, ep, cin, cout, s);
+  if (cin == 32) return launch_cl<NPAD, 32>(m, feats, w, f16, ep, cin, cout, s);
+  return launch_cl<NPAD, 64>(m, feats, w, f16, ep, cin, cout, s);
 }
 
 }  // namespace
@@ -930,15 +946,15 @@ bool conv_tc_supported(int cin, int cout) {
   return cin_ok && cout_ok;
 }
 
-cudaError_t launch_conv_tc_bf16(const sc_map* m, const void* feats, const void* w,
-                                const Epilogue& ep, int cin, int cout, cudaStream_t s) {
+cudaError_t launch_conv_tc(const sc_map* m, const void* feats, const void* w, bool f16,
+                           const Epilogue& ep, int cin, int cout, cudaStream_t s) {
   if (!conv_tc_supported(cin, cout)) return cudaErrorNotSupported;
   const int npad = (cout + 63) / 64 * 64;
   switch (npad) {
-    case 64: return launch_npad<64>(m, feats, w, ep, cin, cout, s);
-    case 128: return launch_npad<128>(m, feats, w, ep, cin, cout, s);
-    case 192: return launch_npad<192>(m, feats, w, ep, cin, cout, s);
-    default: return launch_npad<256>(m, feats, w, ep, cin, cout, s);
+    case 64: return launch_npad<64>(m, feats, w, f16, ep, cin, cout, s);
+    case 128: return launch_npad<128>(m, feats, w, f16, ep, cin, cout, s);
+    case 192: return launch_npad<192>(m, feats, w, f16, ep, cin, cout, s);
+    default: return launch_npad<256>(m, feats, w, f16, ep, cin, cout, s);
   }
 }
 

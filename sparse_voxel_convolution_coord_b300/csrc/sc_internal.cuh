@@ -370,12 +370,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
   return d;
 }
 
-// Instruction descriptor: kind::f16, A = B = bf16, D = fp32, A K-major,
-// B MN-major (row-major W[k][ci][co] has co contiguous), shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
+// Instruction descriptor: kind::f16, A = B = bf16 (or both fp16), D = fp32,
+// A K-major, B MN-major (row-major W[k][ci][co] has co contiguous), M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool f16 = false) {
   return (1u << 4)                      // D format fp32
-         | (1u << 7)                    // A format bf16
-         | (1u << 10)                   // B format bf16
+         | ((f16 ? 0u : 1u) << 7)       // A format: 0 fp16, 1 bf16
+         | ((f16 ? 0u : 1u) << 10)      // B format: the same as A
          | (0u << 15)                   // A K-major
          | (1u << 16)                   // B MN-major
          | ((uint32_t)(n >> 3) << 17)   // N / 8
@@ -424,14 +424,16 @@ size_t pairs_scratch_bytes(int64_t n);
 // The convolution's fused epilogue ("Porting TRELLIS.2 From Python to Rust
 // and Metal", section V: bias, rounding, activation and the residual add in
 // the same pass): out = act(acc + bias) + residual, in fp32, then stored as
-// fp32 or rounded to bf16 (nearest, ties to even).
+// fp32 or rounded to bf16 / fp16 (nearest, ties to even).
 struct Epilogue {
   const float* bias;     // [cout] or nullptr
   const void* residual;  // [n][cout] in the output dtype, or nullptr
   void* out;             // [n][cout]
   int act;               // SC_ACT_NONE / SC_ACT_RELU / SC_ACT_SILU
-  int out_bf16;          // 1: bf16 output, 0: fp32
+  int out_half;          // output: 0 fp32, kOutBf16, kOutF16
 };
+constexpr int kOutBf16 = 1;
+constexpr int kOutF16 = 2;
 
 __device__ __forceinline__ float apply_act(float v, int act) {
   if (act == SC_ACT_RELU) return fmaxf(v, 0.f);
@@ -443,9 +445,10 @@ __device__ __forceinline__ float apply_act(float v, int act) {
 
 cudaError_t launch_conv_simt_f32(const sc_map* m, const float* feats, const float* w,
                                  const Epilogue& ep, int cin, int cout, cudaStream_t s);
-// Returns cudaErrorNotSupported for shapes outside the tensor-core envelope.
-cudaError_t launch_conv_tc_bf16(const sc_map* m, const void* feats, const void* w,
-                                const Epilogue& ep, int cin, int cout, cudaStream_t s);
+// bf16 or fp16 operands (f16 = true); returns cudaErrorNotSupported for
+// shapes outside the tensor-core envelope.
+cudaError_t launch_conv_tc(const sc_map* m, const void* feats, const void* w, bool f16,
+                           const Epilogue& ep, int cin, int cout, cudaStream_t s);
 bool conv_tc_supported(int cin, int cout);
 // Process-wide count of the kernels this library has launched (host side).
 void note_launches(int k);

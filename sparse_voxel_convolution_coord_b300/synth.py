@@ -224,6 +224,10 @@ def make_tensors(n: int, cin: int, cout: int, dtype: str, seed_key: int):
     bias = (rw.standard_normal(cout) * 0.1).astype(np.float32)
     if dtype == "bf16":
         feats, weight = round_bf16(feats), round_bf16(weight)
+    elif dtype == "f16":
+        # numpy's float16 conversion rounds to nearest, ties to even
+        feats = feats.astype(np.float16).astype(np.float32)
+        weight = weight.astype(np.float16).astype(np.float32)
     elif dtype != "f32":
         raise ValueError(dtype)
     return feats, weight, bias

@@ -43,8 +43,11 @@ def gpu_map(sc, coords, res):
     return m, nbr
 
 
+TORCH_DT = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+
+
 def gpu_conv(sc, m, feats, weight, bias, dtype):
-    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    tdt = TORCH_DT[dtype]
     out = sc.sc_forward(m, to_dev(feats, tdt), to_dev(weight, tdt),
                         None if bias is None else to_dev(bias))
     sc.sc_device_status(m)
@@ -57,7 +60,7 @@ def assert_close(got, ref, dtype, what=""):
     rel = np.linalg.norm(err) / max(nref, 1e-300)
     if dtype == "f32":
         assert rel <= F32_REL_L2, "%s rel L2 %.3e > %.0e" % (what, rel, F32_REL_L2)
-    else:
+    else:  # bf16 and fp16 inputs: the half-precision bars
         rms = nref / np.sqrt(ref.size)
         mx = np.abs(err).max() if err.size else 0.0
         assert rel <= BF16_REL_L2, "%s rel L2 %.3e" % (what, rel)
@@ -231,6 +234,29 @@ def test_conv_bf16_shapes(sc, cin, cout):
     check_problem(sc, coords, 14, feats, weight, bias, "bf16", what="%dx%d" % (cin, cout))
 
 
+@pytest.mark.parametrize("cin,cout", [(16, 16), (64, 192), (256, 256), (32, 256)])
+def test_conv_f16_shapes(sc, cin, cout):
+    """fp16 operands on the tensor cores (tcgen05 kind::f16 with fp16 A and B)."""
+    rng = np.random.default_rng(cin * 1000 + cout + 1)
+    coords = random_coords(rng, 2, 14, 0.25)
+    feats, weight, bias = synth.make_tensors(len(coords), cin, cout, "f16", cin + cout)
+    check_problem(sc, coords, 14, feats, weight, bias, "f16", what="f16 %dx%d" % (cin, cout))
+
+
+@pytest.mark.parametrize("key", [2, 3])
+def test_conv_f16_configs(sc, key):
+    """Configs 2 and 3 with their inputs rounded to fp16 instead of bf16."""
+    p = synth.make_problem(key)
+    feats, weight, bias = synth.make_tensors(p.n, p.feats.shape[1], p.weight.shape[2], "f16", key)
+    rows = None
+    if key == 3:
+        rng = np.random.default_rng(44)
+        rows = np.unique(np.concatenate([np.arange(0, 256), np.arange(p.n - 300, p.n),
+                                         rng.choice(p.n, size=3000, replace=False)]))
+    check_problem(sc, p.coords, p.res, feats, weight, bias, "f16", rows=rows,
+                  what="f16 config %d" % key)
+
+
 @pytest.mark.parametrize("cin,cout", [(32, 32), (3, 5), (100, 256), (64, 128)])
 def test_conv_f32_shapes(sc, cin, cout):
     rng = np.random.default_rng(cin + 7 * cout)
@@ -355,46 +381,50 @@ def _oracle_conv_full(key):
     return _ORACLE_CONV[key]
 
 
-def bf16_ulp(x):
-    """Spacing of bf16 values at |x| (2^-133 below fp32's normal range)."""
+def half_ulp(x, odt):
+    """Spacing of bf16 (8 significant bits, 2^-133 below 2^-126) or fp16 (11
+    significant bits, 2^-24 below 2^-14) values at |x|."""
+    sig, emin = (8, -125) if odt == "bf16" else (11, -13)
     _, e = np.frexp(np.abs(x))
-    return np.ldexp(1.0, np.maximum(e, -125) - 8)
+    return np.ldexp(1.0, np.maximum(e, emin) - sig)
 
 
 def check_epilogue_out(got, ref, odt, in_dtype, what):
-    """fp32 output: the convolution's bars.  bf16 output: within one bf16
-    spacing of the oracle's value rounded to bf16 (the GPU rounds its fp32
-    result, which can sit on the other side of a rounding boundary), plus the
-    fp32 accumulation error, and equal to it for nearly every element."""
+    """fp32 output: the convolution's bars.  bf16 / fp16 output: within one
+    spacing of the oracle's value rounded to that format (the GPU rounds its
+    fp32 result, which can sit on the other side of a rounding boundary),
+    plus the fp32 accumulation error, and equal to it for nearly every element
+    (fp16's finer spacing leaves more elements near a boundary)."""
     if odt == "f32":
         assert_close(got, ref, in_dtype, what)
         return
-    rref = oracle.round_bf16(ref)
+    rref = oracle.round_bf16(ref) if odt == "bf16" else oracle.round_f16(ref)
     rms = np.linalg.norm(ref) / np.sqrt(ref.size)
     err = np.abs(got - rref)
-    bound = bf16_ulp(ref) + 1e-4 * rms
-    assert np.all(err <= bound), "%s: %d elements beyond one bf16 spacing" % (
-        what, int((err > bound).sum()))
+    bound = half_ulp(ref, odt) + 1e-4 * rms
+    assert np.all(err <= bound), "%s: %d elements beyond one %s spacing" % (
+        what, int((err > bound).sum()), odt)
     frac = np.mean(got == rref)
-    assert frac >= 0.95, "%s: only %.3f of elements equal the rounded oracle" % (what, frac)
+    floor = 0.95 if odt == "bf16" else 0.9
+    assert frac >= floor, "%s: only %.3f of elements equal the rounded oracle" % (what, frac)
 
 
 def _residual(n, cout, odt, seed):
     r = np.random.default_rng(seed).standard_normal((n, cout)).astype(np.float32)
-    if odt == "bf16":
-        r = torch.from_numpy(r).to(torch.bfloat16).to(torch.float32).numpy()
+    if odt != "f32":
+        r = torch.from_numpy(r).to(TORCH_DT[odt]).to(torch.float32).numpy()
     return r
 
 
 @pytest.mark.parametrize("key", [1, 2])
 @pytest.mark.parametrize("act", ["none", "relu", "silu"])
 @pytest.mark.parametrize("resid", [False, True])
-@pytest.mark.parametrize("odt", ["f32", "bf16"])
+@pytest.mark.parametrize("odt", ["f32", "bf16", "f16"])
 def test_fused_epilogue(sc, key, act, resid, odt):
     p = synth.make_problem(key)
     cout = p.weight.shape[2]
-    tin = torch.bfloat16 if p.config.dtype == "bf16" else torch.float32
-    tout = torch.bfloat16 if odt == "bf16" else torch.float32
+    tin = TORCH_DT[p.config.dtype]
+    tout = TORCH_DT[odt]
     r = _residual(p.n, cout, odt, 100 + key) if resid else None
     m, _ = gpu_map(sc, p.coords, p.res)
     out = sc.sc_forward_ex(m, to_dev(p.feats, tin), to_dev(p.weight, tin), to_dev(p.bias),
@@ -409,14 +439,15 @@ def test_fused_epilogue(sc, key, act, resid, odt):
         key, act, resid, odt))
 
 
-@pytest.mark.parametrize("act,odt", [("none", "f32"), ("silu", "bf16"), ("relu", "f32")])
+@pytest.mark.parametrize("act,odt", [("none", "f32"), ("silu", "bf16"), ("relu", "f32"),
+                                     ("none", "f16")])
 def test_fused_epilogue_split_shapes(sc, act, odt):
     """64^3, C=256: with act none and fp32 output the last partial round of
     tiles is split and its parts add the residual in the last part; an
     activation or bf16 output runs unsplit."""
     p = synth.make_problem(3)
     cout = p.weight.shape[2]
-    tout = torch.bfloat16 if odt == "bf16" else torch.float32
+    tout = TORCH_DT[odt]
     r = _residual(p.n, cout, odt, 7)
     m, nbr = gpu_map(sc, p.coords, p.res)
     out = sc.sc_forward_ex(m, to_dev(p.feats, torch.bfloat16), to_dev(p.weight, torch.bfloat16),

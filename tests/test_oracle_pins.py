@@ -374,28 +374,64 @@ def check_round_bf16_against_torch(rnd):
     np.testing.assert_array_equal(rnd(x.astype(np.float64)), want)
 
 
+def check_round_f16(rnd):
+    u = 2.0 ** -10  # binary16 spacing in [1, 2)
+    cases = {
+        1.0 + u / 2: 1.0,                   # tie -> even
+        1.0 + 3 * u / 2: 1.0 + 2 * u,       # tie -> even
+        1.0 + u / 2 + 2.0 ** -30: 1.0 + u,
+        65504.0: 65504.0,                   # largest finite
+        65519.0: 65504.0,                   # below the tie with 2^16
+        65520.0: np.inf,                    # the tie goes to 2^16: infinity
+        2.0 ** -24: 2.0 ** -24,             # smallest subnormal
+        2.0 ** -25: 0.0,                    # tie between 0 and 2^-24 -> 0 (even)
+        3 * 2.0 ** -26: 2.0 ** -24,
+        -(2.0 ** -14) * 1.5: -(2.0 ** -14) * 1.5,
+        1.0 / 3.0: float.fromhex("0x1.554p-2"),
+    }
+    got = rnd(np.array(list(cases.keys())))
+    np.testing.assert_array_equal(got, np.array(list(cases.values())))
+
+
+def check_round_f16_against_numpy(rnd):
+    # numpy's float64 -> float16 conversion rounds to nearest even directly
+    # (an independent implementation)
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal(20000) * np.exp(rng.uniform(-20, 12, 20000))
+    with np.errstate(over="ignore"):
+        want = x.astype(np.float16).astype(np.float64)
+    np.testing.assert_array_equal(rnd(x), want)
+
+
 EPILOGUE_CHECKS = [
-    lambda a, e, r: check_activation(a),
-    lambda a, e, r: check_epilogue(e),
-    lambda a, e, r: check_round_bf16(r),
-    lambda a, e, r: check_round_bf16_against_torch(r),
+    lambda a, e, r, h: check_activation(a),
+    lambda a, e, r, h: check_epilogue(e),
+    lambda a, e, r, h: check_round_bf16(r),
+    lambda a, e, r, h: check_round_bf16_against_torch(r),
+    lambda a, e, r, h: check_round_f16(h),
+    lambda a, e, r, h: check_round_f16_against_numpy(h),
 ]
 
 
 def test_epilogue_pins():
     for chk in EPILOGUE_CHECKS:
-        chk(oracle.activation, oracle.epilogue, oracle.round_bf16)
+        chk(oracle.activation, oracle.epilogue, oracle.round_bf16, oracle.round_f16)
 
 
-def _mutant_round(mode):
+def _mutant_round(mode, sig_bits=8, e_min=-125):
     def rnd(v):
         v = np.asarray(v, np.float64)
         out = np.zeros_like(v)
         nz = (v != 0.0) & np.isfinite(v)
         _, e = np.frexp(v[nz])
-        step = np.ldexp(1.0, np.maximum(e, -125) - 8)
+        step = np.ldexp(1.0, np.maximum(e, e_min) - sig_bits)
         t = v[nz] / step
-        q = np.trunc(t) if mode == "truncate" else np.sign(t) * np.floor(np.abs(t) + 0.5)
+        if mode == "truncate":
+            q = np.trunc(t)
+        elif mode == "even":
+            q = np.rint(t)
+        else:  # ties away from zero
+            q = np.sign(t) * np.floor(np.abs(t) + 0.5)
         out[nz] = q * step
         out[~nz] = v[~nz]
         return out
@@ -407,13 +443,19 @@ EPILOGUE_MUTANTS = {
         oracle.activation,
         lambda v, act=0, residual=None: oracle.activation(
             np.asarray(v, np.float64) + (0.0 if residual is None else residual), act),
-        oracle.round_bf16),
+        oracle.round_bf16, oracle.round_f16),
     "silu_sign_slip": (
         lambda v, act: (np.asarray(v, np.float64) / (1.0 + np.exp(np.asarray(v, np.float64)))
                         if act == oracle.ACT_SILU else oracle.activation(v, act)),
-        oracle.epilogue, oracle.round_bf16),
-    "round_ties_away": (oracle.activation, oracle.epilogue, _mutant_round("away")),
-    "round_truncate": (oracle.activation, oracle.epilogue, _mutant_round("truncate")),
+        oracle.epilogue, oracle.round_bf16, oracle.round_f16),
+    "round_ties_away": (oracle.activation, oracle.epilogue, _mutant_round("away"),
+                        oracle.round_f16),
+    "round_truncate": (oracle.activation, oracle.epilogue, _mutant_round("truncate"),
+                       oracle.round_f16),
+    "f16_ties_away": (oracle.activation, oracle.epilogue, oracle.round_bf16,
+                      _mutant_round("away", 11, -13)),
+    "f16_wrong_subnormal_spacing": (oracle.activation, oracle.epilogue, oracle.round_bf16,
+                                    _mutant_round("even", 11, -14)),
 }
 
 
