@@ -1,4 +1,5 @@
-// sc_conv_tc.cu -- bf16 submanifold convolution on the sm_103a tensor cores.
+// sc_conv_tc.cu -- bf16 / fp16 submanifold convolution on the sm_103a tensor
+// cores.
 //
 // What it computes ("Porting TRELLIS.2 From Python to Rust and Metal",
 // section V: a gather-GEMM over the neighbour table with half-precision
@@ -7,14 +8,20 @@
 //
 //   out[o][:] = bias + sum_{k : nbr[o][k] >= 0} feats[nbr[o][k]][:] @ W[k]
 //
+// and, in the FUSED instantiation, the rest of the epilogue in the same pass
+// (the same section: bias, rounding, activation and the residual add):
+// out = act(out) + residual, stored as fp32, bf16 or fp16.
+//
 // How: an output-stationary implicit GEMM.  A CTA owns a tile of 128 output
 // rows; the GEMM's K dimension is (offset, input channel).  For each offset
 // present in the tile (its 27-bit OR mask), the 128 neighbour rows are
 // gathered straight from the feature matrix by cp.async (absent neighbours
 // zero-filled) and W[k] arrives by tiled TMA; a single thread issues
-// tcgen05.mma (M = 128, N = cout padded to 64, K = 16, bf16 x bf16 -> fp32)
-// into a TMEM accumulator.  Each output row belongs to exactly one tile, so
-// the epilogue (TMEM -> registers, + bias, fp32 store) needs no atomics.
+// tcgen05.mma (M = 128, N = cout padded to 64, K = 16, bf16 x bf16 or fp16 x
+// fp16 -> fp32; the instruction descriptor is a launch argument) into a TMEM
+// accumulator.  Each output row belongs to exactly one tile, so the epilogue
+// (TMEM -> registers -> shared staging -> coalesced stores) needs no atomics,
+// except in the tail split below.
 //
 // Tail split: the grid is persistent (one cluster per pair of SMs), so when
 // the units do not divide evenly over the clusters the last, partial wave
@@ -40,8 +47,9 @@
 // CTA = 14 warps, persistent over units of CL tiles:
 //   warps 0-3  epilogue (warp q reads TMEM lanes 32q..32q+31 = rows of the tile)
 //   warp 4     loader: the tile's 128 x 27 neighbour block by one bulk copy
-//              (double-buffered, one unit ahead) and, per stage, this CTA's
-//              W boxes by tiled TMA
+//              (two buffers, one unit ahead, for cout <= 64; one buffer,
+//              refilled after a unit's stages, above) and, per stage, this
+//              CTA's W boxes by tiled TMA
 //   warps 5-12 A producers: per pipeline stage the 256 threads gather the
 //              A rows with 16-byte cp.async copies (consecutive threads take
 //              consecutive 16-byte chunks of a row, so a warp instruction
@@ -55,9 +63,11 @@
 // main loop.  Every wait is bounded (~2 s): a CTA that gives up records
 // SC_ERR_DEVICE_TIMEOUT in the map's status word and leaves cleanly.
 //
-// Shared-memory operand layouts (both built by TMA swizzling):
+// Shared-memory operand layouts (A written swizzled by the producers'
+// cp.async addresses, B by TMA swizzling):
 //   A (gathered rows, K-major): per stage 64/CS segments, each 128 rows x CS
-//     bf16, rows of 2*CS bytes with the matching 128/64/32-byte swizzle;
+//     16-bit values, rows of 2*CS bytes with the matching 128/64/32-byte
+//     swizzle;
 //   B (W[k] rows, MN-major): per stage [cout/64 blocks][64 K rows][128 B],
 //     128-byte swizzle; LBO = 8 KB between 64-column blocks, SBO = 1 KB
 //     between 8-row groups.
