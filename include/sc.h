@@ -53,8 +53,8 @@ typedef enum {
   SC_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, bad alignment, ... */
   SC_ERR_COORD_RANGE = 2,  /* a coordinate outside [0,res) or a negative batch  */
   SC_ERR_DUPLICATE = 3,    /* two rows with the same (b,x,y,z)                  */
-  SC_ERR_TABLE_FULL = 4,   /* hash probe bound exceeded (cannot happen at the
-                              library's load factor <= 1/2 unless forced)       */
+  SC_ERR_TABLE_FULL = 4,   /* hash probe bound exceeded (cannot happen: the
+                              table's load factor is at most 1/2)               */
   SC_ERR_UNSUPPORTED = 5,  /* shape/dtype outside the kernels' envelope         */
   SC_ERR_ALLOC = 6,        /* device allocation failed                          */
   SC_ERR_CUDA = 7,         /* a CUDA runtime/driver call failed                 */
@@ -176,9 +176,10 @@ SC_API sc_status sc_set_deterministic(int32_t enable);
 
 /*
  * Number of GPU kernels this library has launched in this process, counted on
- * the host at each launch (map build: 3 per sc_build_map; sc_forward: 1, or 2
- * when the bf16 path zeroes split rows first; 1 per sc_get_neighbor_table; 3
- * or 4 per sc_get_pairs).  For measuring launches over a region of code.
+ * the host at each launch (map build: 3 per sc_build_map, 6 when it retries
+ * with 64-bit keys; sc_forward: 1, or 2 when the tensor-core path zeroes
+ * split rows first; 1 per sc_get_neighbor_table; 3 or 4 per sc_get_pairs).
+ * For measuring launches over a region of code.
  */
 SC_API uint64_t sc_kernel_launches(void);
 

@@ -216,7 +216,7 @@ sc_handle sc_build_map(const int32_t* coords, int64_t n, int32_t res, void* stre
     // the tile-major neighbour table [ntiles][27][128] (pad rows -1: a
     // tile's rows are contiguous per offset, and a tile's whole 13,824-byte
     // block is one contiguous range for the convolution), the tile masks and
-    // the 16-byte status / pair-count block.
+    // the status / pair-counter block (sc::kStatusBlockBytes).
     auto up = [](size_t b) { return (b + 255) & ~size_t(255); };
     const size_t b_slots = up(cap * sizeof(uint64_t));
     const size_t b_nbr = up((size_t)m->ntiles * sc::kTileRows * sc::kTaps * sizeof(int32_t));

@@ -7,7 +7,8 @@
 // the row of the neighbour voxel or -1.  Here:
 //
 //  k_hash_insert     open addressing over a power-of-two table of packed
-//                    64-bit slots (key << vbits | row) with brick-local home
+//                    64-bit slots (32-bit keys: key << 32 | moved flag << 31 |
+//                    row; otherwise key << vbits | row) with brick-local home
 //                    slots and double-hashing probes (sc_internal.cuh).  The
 //                    warp inserts its 32 keys in synchronous probing rounds:
 //                    in each round every lane whose key is still pending
@@ -287,7 +288,7 @@ __global__ void __launch_bounds__(kTileRows) k_nbr_to_row_major(const int32_t* _
 }
 
 // One launch instead of three memsets: every slot empty (all ones), the
-// tile masks and the 16-byte status / pair-count block zero.
+// tile masks and the status / pair-counter block zero.
 __global__ void __launch_bounds__(256) k_map_init(ulonglong2* __restrict__ slots, int64_t npairs2,
                                                   uint32_t* __restrict__ tile_mask, int64_t ntiles,
                                                   uint32_t* __restrict__ status) {
