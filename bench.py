@@ -153,10 +153,12 @@ def oracle_sample_run(p, rows, threads=0):
     return dt, pairs
 
 
-def cpu_baseline(p, target_s=20.0):
+def cpu_baseline(p, target_s=20.0, single_s=4.0):
     """The oracle as it stands on the host cores, for ~target_s seconds: the
     whole workload (map build + fp64 convolution of every row) repeated while
-    it fits, else the map build and a row sample sized to the target."""
+    it fits, else the map build and a row sample sized to the target.  Also
+    the same oracle on one thread (its map build is single-threaded anyway),
+    on a row sample of ~single_s seconds."""
     import oracle
     cin, cout = p.feats.shape[1], p.weight.shape[2]
     rng = np.random.default_rng(0)
@@ -190,9 +192,18 @@ def cpu_baseline(p, target_s=20.0):
             p.n, m)
         rows_done = m
     tflops = 2.0 * pairs * cin * cout / dt / 1e12
+    # the same oracle on one thread, on a sample of ~single_s seconds
+    per_row1 = per_row * oracle.max_threads()
+    m1 = int(min(p.n, max(64, (single_s - t_map) / per_row1)))
+    rows1 = np.sort(rng.choice(p.n, size=m1, replace=False))
+    dt1, pairs1 = oracle_sample_run(p, rows1, threads=1)
     return {"value": tflops, "unit": "TFLOP/s", "cores": oracle.max_threads(),
             "kind": "oracle",
-            "sample": "%s: %d pairs in %.1f s; voxels/s %.3g" % (what, pairs, dt, rows_done / dt)}
+            "sample": "%s: %d pairs in %.1f s; voxels/s %.3g" % (what, pairs, dt, rows_done / dt),
+            "single_thread": {
+                "value": 2.0 * pairs1 * cin * cout / dt1 / 1e12, "unit": "TFLOP/s", "cores": 1,
+                "sample": "oracle map build over all %d voxels + fp64 conv of %d sampled rows "
+                          "on one thread: %d pairs in %.1f s" % (p.n, m1, pairs1, dt1)}}
 
 
 def run_reference(args):

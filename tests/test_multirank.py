@@ -66,3 +66,14 @@ def test_single_rank_needs_no_process_group():
     assert bench.init_dist(1) is None
     assert bench.max_over_ranks(None, 3.5) == 3.5
     assert bench.whole_job_rate(1, 10.0, 5.0) == pytest.approx(2000.0)
+
+
+def test_cpu_baseline_reports_all_cores_and_one_thread():
+    """bench.py's CPU-oracle leg on the small fp32 workload: a positive rate
+    on all cores and on one thread, each with its sample described."""
+    import bench
+    from sparse_voxel_convolution_coord_b300 import synth
+    cb = bench.cpu_baseline(synth.make_problem(1), target_s=0.5, single_s=0.2)
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1
+    assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
+    assert "whole workload" in cb["sample"] or "sampled" in cb["sample"]
