@@ -277,6 +277,42 @@ def time_forward_alone(sc, torch, m, feats, weight, bias, out, flush, stream, re
     return statistics.median(a.elapsed_time(b) for a, b in evs[10:])
 
 
+def roofline_object(dtype, flops, fwd_bytes, t_kernel_ms, peaks, traffic):
+    """The bench line's roofline for one forward launch of t_kernel_ms: the
+    tensor pipe or HBM, whichever the algorithmic flops or bytes would take
+    longer on (fp16 takes the bf16 measured peak x the nominal fp16/bf16
+    ratio, 1); the fp32 FFMA path against HBM."""
+    t_s = t_kernel_ms * 1e-3
+    if dtype == "f32":
+        gbs = fwd_bytes / t_s / 1e9
+        return {"kernel": "k_conv_simt_f32 (fp32 FFMA gather-GEMM)", "bound": "hbm",
+                "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"] + " hbm",
+                "traffic": None, "kernel_us": t_kernel_ms * 1e3,
+                "algorithmic_bytes_per_launch": fwd_bytes}
+    kernel = "k_conv_tc (gather-implicit-GEMM, tcgen05, %s -> fp32 TMEM)" % dtype
+    tensor_bound = (flops / (peaks["bf16_tflops"] * 1e12)
+                    >= fwd_bytes / (peaks["hbm_gbs"] * 1e9))
+    if tensor_bound:
+        achieved = flops / t_s / 1e12
+        return {"kernel": kernel, "bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"],
+                "frac_of_sustained": (achieved / peaks["bf16_tflops_sustained"]
+                                      if peaks.get("bf16_tflops_sustained") else None),
+                "peak_source": peaks["source"] + " bf16 burst (MEASURED_PEAKS.json)"
+                               + (" x nominal fp16/bf16 ratio 1" if dtype == "f16" else ""),
+                "traffic": traffic, "kernel_us": t_kernel_ms * 1e3,
+                "algorithmic_flops_per_launch": flops,
+                "algorithmic_bytes_per_launch": fwd_bytes}
+    gbs = fwd_bytes / t_s / 1e9
+    return {"kernel": kernel, "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+            "peak_source": peaks["source"] + " hbm", "traffic": traffic,
+            "kernel_us": t_kernel_ms * 1e3, "algorithmic_flops_per_launch": flops,
+            "tensor_tflops": flops / t_s / 1e12, "algorithmic_bytes_per_launch": fwd_bytes}
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
@@ -290,8 +326,8 @@ def run_ours(args):
 
     p = synth.make_problem(args.config)
     cin, cout = p.feats.shape[1], p.weight.shape[2]
-    tdt = torch.bfloat16 if p.config.dtype == "bf16" else torch.float32
-    esize = 2 if p.config.dtype == "bf16" else 4
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[p.config.dtype]
+    esize = 4 if p.config.dtype == "f32" else 2
     coords = torch.from_numpy(p.coords).to(dev)
     feats = torch.from_numpy(p.feats).to(dev).to(tdt)
     weight = torch.from_numpy(p.weight).to(dev).to(tdt)
@@ -398,26 +434,9 @@ def run_ours(args):
     conv_src = os.path.join(ROOT, "sparse_voxel_convolution_coord_b300", "csrc", "sc_conv_tc.cu")
     traffic = None
     rec = MEASURED_TRAFFIC.get(p.config.name)
-    if rec is not None and p.config.dtype == "bf16" and rec[0] == _file_sha1(conv_src):
+    if rec is not None and p.config.dtype != "f32" and rec[0] == _file_sha1(conv_src):
         traffic = rec[1]
-    if p.config.dtype == "bf16":
-        achieved = flops / (t_kernel * 1e-3) / 1e12
-        roofline = {"kernel": "k_conv_tc (gather-implicit-GEMM, tcgen05, bf16 -> fp32 TMEM)",
-                    "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                    "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                    "frac_of_sustained": (achieved / peaks["bf16_tflops_sustained"]
-                                          if peaks.get("bf16_tflops_sustained") else None),
-                    "peak_source": peaks["source"] + " bf16 burst (MEASURED_PEAKS.json)",
-                    "traffic": traffic, "kernel_us": t_kernel * 1e3,
-                    "algorithmic_flops_per_launch": flops,
-                    "algorithmic_bytes_per_launch": fwd_bytes}
-    else:
-        gbs = fwd_bytes / (t_kernel * 1e-3) / 1e9
-        roofline = {"kernel": "k_conv_simt_f32 (fp32 FFMA gather-GEMM)", "bound": "hbm",
-                    "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"] + " hbm",
-                    "traffic": None, "kernel_us": t_kernel * 1e3,
-                    "algorithmic_bytes_per_launch": fwd_bytes}
+    roofline = roofline_object(p.config.dtype, flops, fwd_bytes, t_kernel, peaks, traffic)
     build_gbs = build_bytes / (t_build * 1e-3) / 1e9
     line = {
         "metric": METRIC,
@@ -426,7 +445,7 @@ def run_ours(args):
         "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": t_step_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if p.config.dtype == "bf16" else "f32",
+        "dtype": p.config.dtype,
         "data": "synthetic (seeded superquadric voxel shells; random N(0,1) features, "
                 "N(0, 1/sqrt(27 cin)) weights)",
         "config": {"workload": p.config.name, "description": p.config.description,

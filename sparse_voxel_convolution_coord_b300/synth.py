@@ -24,6 +24,14 @@ Recipe (the pages fix none of it; this is the reading taken):
     "inside, and some cell of the (2t+1)^3 cube around it is outside";
   * a union of shapes is the union of their individual shells;
   * extra "noise" sites are drawn uniformly from the empty cells;
+  * decoder scale (1024^3, millions of voxels, as the pages' shape decoders
+    produce from a 64^3 structure by repeated subdivision): the 1-voxel shell
+    of one superquadric found by sparse refinement.  The 64^3 cells the
+    surface crosses are split into 8 children per level, keeping the
+    children whose cube (grown by one fine voxel) straddles the surface by
+    the field's values at its corners and centre; at full resolution the
+    1-shell rule above is applied exactly, by evaluating the field at each
+    candidate's 26 neighbours;
   * rows are listed in (batch, x, y, z) lexicographic order, the order an
     argwhere over an occupancy grid produces;
   * features ~ N(0, 1); weights ~ N(0, 1/sqrt(27 * cin)) (standard deviation);
@@ -52,7 +60,7 @@ class Config:
     res: int
     cin: int
     cout: int
-    dtype: str          # "f32" or "bf16": the dtype of feats and weights
+    dtype: str          # "f32", "bf16" or "f16": the dtype of feats and weights
     description: str
 
 
@@ -72,6 +80,9 @@ CONFIGS = {
     5: Config(5, "sq4x256_400k_c32_bf16", 1, 256, 32, 32, "bf16",
               "batch 1, 256^3, union of 4 superquadric 1-voxel shells (~396k) "
               "plus 1% random sites, C=32, bf16"),
+    6: Config(6, "sq1024_dec_c64_f16", 1, 1024, 64, 64, "f16",
+              "batch 1, 1024^3, 1-voxel shell of one superquadric refined from "
+              "64^3 (millions of voxels, decoder scale), C=64, fp16"),
 }
 
 
@@ -152,6 +163,158 @@ def superquadric_shells(res: int, n_shapes: int, target: int, t: int,
     return _bisect_scale(bounds, target, res)
 
 
+class SuperquadricField:
+    """The radius-like superquadric field G = F^(e1/2) at unit scale,
+    evaluated at arbitrary points (inside at scale s iff G <= s)."""
+
+    def __init__(self, rng: np.random.Generator, centre):
+        self.e1, self.e2 = rng.uniform(0.5, 3.0, size=2)
+        self.axes = rng.uniform(0.5, 1.0, size=3)
+        self.rot = random_rotation(rng)
+        self.centre = np.asarray(centre, dtype=np.float64)
+
+    def __call__(self, pts: np.ndarray) -> np.ndarray:
+        d = np.asarray(pts, dtype=np.float64) - self.centre
+        pj = np.abs(d @ self.rot) / self.axes          # p' = R^T (p - c), per axis
+        e1, e2 = self.e1, self.e2
+        f = (pj[:, 0] ** (2.0 / e2) + pj[:, 1] ** (2.0 / e2)) ** (e2 / e1) + pj[:, 2] ** (2.0 / e1)
+        return f ** (e1 / 2.0)
+
+
+_CUBE = np.array([[i, j, k] for i in (0, 1) for j in (0, 1) for k in (0, 1)], np.int64)
+def _lattice(m: int) -> np.ndarray:
+    t = np.arange(m, dtype=np.float64) / (m - 1)
+    return np.stack(np.meshgrid(t, t, t, indexing="ij"), axis=-1).reshape(-1, 3)
+
+
+_LATTICE3 = _lattice(3)
+_LATTICE5 = _lattice(5)
+_NEIGH27 = np.array([[i, j, k] for i in (-1, 0, 1) for j in (-1, 0, 1) for k in (-1, 0, 1)],
+                    np.int64)  # index 13 is the cell itself
+
+
+def _straddles(field, scale, cells: np.ndarray, h: int, res: int) -> np.ndarray:
+    """Cells (of side h fine voxels, fine-grid origin h * cell) whose cube,
+    grown by 1 + h / 2 fine voxels on every side, has field values on both
+    sides of `scale` on an evenly spaced lattice over it (5 x 5 x 5 points
+    for h >= 8, else 3 x 3 x 3; points off the grid count as outside, as in
+    the shell rule)."""
+    lat = _LATTICE5 if h >= 8 else _LATTICE3
+    g0 = 1 + h // 2
+    lo = (cells * h - g0).astype(np.float64)
+    span = float(h - 1 + 2 * g0)
+    pts = (lo[:, None, :] + lat[None, :, :] * span).reshape(-1, 3)
+    g = field(np.clip(pts, 0, res - 1))
+    g[((pts < 0) | (pts > res - 1)).any(axis=1)] = np.inf  # off the grid is outside
+    g = g.reshape(len(cells), len(lat))
+    return (g.min(axis=1) <= scale) & (g.max(axis=1) > scale)
+
+
+def _shell_rule(field, scale, cells: np.ndarray, res: int) -> np.ndarray:
+    """The exact 1-shell rule on fine cells: inside (G <= scale) with some
+    cell of the 3x3x3 cube around it outside (G > scale, or off the grid)."""
+    nb = (cells[:, None, :] + _NEIGH27[None, :, :]).reshape(-1, 3)
+    off_grid = ((nb < 0) | (nb >= res)).any(axis=1).reshape(len(cells), 27)
+    g = field(np.clip(nb, 0, res - 1)).reshape(len(cells), 27)
+    return (g[:, 13] <= scale) & (off_grid | (g > scale)).any(axis=1)
+
+
+_BLOCK4 = np.array([[i, j, k] for i in range(-1, 3) for j in range(-1, 3) for k in range(-1, 3)],
+                   np.int64)
+
+
+def _shell_rule_blocks(field, scale, parents: np.ndarray, res: int) -> np.ndarray:
+    """The exact 1-shell rule on the 8 children (2p + {0,1}^3) of each parent
+    p, from one evaluation of the field on the parent's 4x4x4 neighbourhood
+    (2p + {-1..2}^3) instead of 27 per child.  Returns [nP, 8] booleans in
+    _CUBE order."""
+    pts = (parents[:, None, :] * 2 + _BLOCK4[None, :, :]).reshape(-1, 3)
+    off = ((pts < 0) | (pts >= res)).any(axis=1)
+    g = field(np.clip(pts, 0, res - 1))
+    out = (off | (g > scale)).reshape(-1, 4, 4, 4)
+    g = g.reshape(-1, 4, 4, 4)
+    res_ = np.zeros((len(parents), 8), bool)
+    for c, (i, j, k) in enumerate(_CUBE):
+        win = out[:, i:i + 3, j:j + 3, k:k + 3].reshape(len(parents), 27)
+        res_[:, c] = (g[:, i + 1, j + 1, k + 1] <= scale) & win.any(axis=1)
+    return res_
+
+
+def refined_shell(res: int, base: int, field, scale: float) -> np.ndarray:
+    """int64 [M,3] fine cells of the 1-voxel shell of {G <= scale} on a res^3
+    grid, found from the base^3 cells the surface crosses by splitting each
+    kept cell into 8 per level (res / base a power of two): coarse cells are
+    kept when they straddle the surface, fine cells by the exact rule.  Cells
+    are in (x, y, z) lexicographic order."""
+    ax = np.arange(base, dtype=np.int64)
+    cells = np.stack(np.meshgrid(ax, ax, ax, indexing="ij"), axis=-1).reshape(-1, 3)
+    h = res // base
+    chunk = 1 << 18
+
+    def keep_where(test, cs, *args):
+        keep = np.zeros(len(cs), bool)
+        for a in range(0, len(cs), chunk):
+            keep[a:a + chunk] = test(field, scale, cs[a:a + chunk], *args)
+        return cs[keep]
+
+    if h == 1:
+        cells = keep_where(_shell_rule, cells, res)
+    else:
+        cells = keep_where(_straddles, cells, h, res)
+    while h > 1:
+        h //= 2
+        if h == 1:  # the children of each kept cell at once
+            found = []
+            for a in range(0, len(cells), chunk // 8):
+                par = cells[a:a + chunk // 8]
+                keep = _shell_rule_blocks(field, scale, par, res)
+                kids = par[:, None, :] * 2 + _CUBE[None, :, :]
+                found.append(kids[keep])
+            cells = np.concatenate(found) if found else np.zeros((0, 3), np.int64)
+        else:
+            kids = (cells[:, None, :] * 2 + _CUBE[None, :, :]).reshape(-1, 3)
+            cells = keep_where(_straddles, kids, h, res)
+    order = np.lexsort((cells[:, 2], cells[:, 1], cells[:, 0]))
+    return cells[order]
+
+
+def dense_shell(res: int, field, scale: float) -> np.ndarray:
+    """The same 1-voxel shell from a dense res^3 evaluation (small res only):
+    inside minus its erosion by the 3x3x3 cube, outside the grid counting as
+    outside."""
+    g = field(_grid_points(res)).reshape(res, res, res)
+    inside = g <= scale
+    eroded = ndimage.binary_erosion(inside, structure=np.ones((3, 3, 3), bool),
+                                    iterations=1, border_value=0)
+    return np.argwhere(inside & ~eroded).astype(np.int64)
+
+
+def decoder_scale_shell(res: int, base: int, target_base: int,
+                        rng: np.random.Generator) -> np.ndarray:
+    """One superquadric's 1-voxel shell at res^3 by refinement from base^3,
+    its scale bisected so that the base^3 1-shell holds ~target_base cells
+    (the fine count then grows with (res / base)^2)."""
+    centre = np.full(3, (res - 1) / 2.0)
+    field = SuperquadricField(rng, centre)
+    pts = (_grid_points(base) + 0.5) * (res / base) - 0.5   # base-cell centres, fine units
+    g = field(pts).reshape(base, base, base)
+    lo_s, hi_s = 0.0, 2.0 * res
+    scale = 0.5 * (lo_s + hi_s)
+    for _ in range(60):
+        scale = 0.5 * (lo_s + hi_s)
+        inside = g <= scale
+        shell = inside & ~ndimage.binary_erosion(inside, structure=np.ones((3, 3, 3), bool),
+                                                  iterations=1, border_value=0)
+        cnt = int(shell.sum())
+        if abs(cnt - target_base) <= 0.03 * target_base:
+            break
+        if cnt < target_base:
+            lo_s = scale
+        else:
+            hi_s = scale
+    return refined_shell(res, base, field, scale)
+
+
 def ball_shell(res: int, centre, radius: float) -> np.ndarray:
     p = _grid_points(res) - np.asarray(centre, dtype=np.float64)
     inside = ((p * p).sum(axis=1) <= radius * radius).reshape(res, res, res)
@@ -180,7 +343,7 @@ _COORD_CACHE: dict = {}
 
 
 def make_coords(key: int) -> np.ndarray:
-    """int32 [N,4] (b,x,y,z) coordinates of configuration `key` (1..5)."""
+    """int32 [N,4] (b,x,y,z) coordinates of configuration `key` (1..6)."""
     if key in _COORD_CACHE:
         return _COORD_CACHE[key]
     cfg = CONFIGS[key]
@@ -200,6 +363,12 @@ def make_coords(key: int) -> np.ndarray:
         occ = superquadric_shells(256, 4, 396000, 1, rng, 0.15)
         occ = _add_random_sites(occ, int(round(0.01 * 396000)), rng)
         grids = [occ]
+    elif key == 6:
+        xyz = decoder_scale_shell(1024, 64, 12000, rng)
+        coords = np.ascontiguousarray(
+            np.concatenate([np.zeros((len(xyz), 1), np.int64), xyz], axis=1), dtype=np.int32)
+        _COORD_CACHE[key] = coords
+        return coords
     else:
         raise KeyError(key)
     coords = _coords_of(grids)

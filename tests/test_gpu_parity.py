@@ -481,3 +481,27 @@ def test_forward_ex_rejects_bad_epilogue_arguments(sc):
                              P(out.data_ptr()), f.shape[1], out.shape[1], sc.SC_F32,
                              sc.SC_ACT_NONE, sc.SC_F32, None) == sc.SC_ERR_INVALID_ARG
     m.free()
+
+
+def test_decoder_scale_config():
+    """1024^3, 3.26M voxels, C=64 fp16 (the decoder-scale workload): the whole
+    neighbour map bit-exact, outputs on sampled rows (first tile, ragged last
+    tile, 3,000 random rows) within the half-precision bars."""
+    import sparse_voxel_convolution_coord_b300 as scm
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    p = synth.make_problem(6)
+    m, nbr = gpu_map(scm, p.coords, p.res)
+    want = oracle.build_neighbor_table(p.coords, p.res)
+    np.testing.assert_array_equal(nbr, want)
+    assert scm.sc_map_pairs(m) == int((want >= 0).sum())
+    out = scm.sc_forward(m, to_dev(p.feats, torch.float16), to_dev(p.weight, torch.float16),
+                         to_dev(p.bias))
+    scm.sc_device_status(m)
+    rng = np.random.default_rng(66)
+    rows = np.unique(np.concatenate([np.arange(0, 256), np.arange(p.n - 300, p.n),
+                                     rng.choice(p.n, size=3000, replace=False)]))
+    got = out[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64)
+    m.free()
+    ref = oracle.conv(want[rows], p.feats, p.weight, p.bias)
+    assert_close(got, ref, "f16", "config 6")

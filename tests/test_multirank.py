@@ -77,3 +77,26 @@ def test_cpu_baseline_reports_all_cores_and_one_thread():
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1
     assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
     assert "whole workload" in cb["sample"] or "sampled" in cb["sample"]
+
+
+@pytest.mark.parametrize("key,bound", [(3, "tensor"), (5, "hbm"), (1, "hbm")])
+def test_roofline_takes_the_binding_limit(key, bound):
+    """64^3 C=256 is bound by the tensor pipe, 256^3 C=32 by HBM (its
+    algorithmic bytes take longer than its flops at the measured peaks), the
+    fp32 path is reported against HBM."""
+    import bench
+    from sparse_voxel_convolution_coord_b300 import synth
+    cfg = synth.CONFIGS[key]
+    p = synth.make_problem(key)
+    cin, cout = cfg.cin, cfg.cout
+    es = 4 if cfg.dtype == "f32" else 2
+    pairs = 20 * p.n
+    flops = 2.0 * pairs * cin * cout
+    fwd_bytes = p.n * cin * es + 108 * p.n + 4 * p.n * cout + 27 * cin * cout * es
+    peaks = {"hbm_gbs": 6491.5, "bf16_tflops": 1804.9, "bf16_tflops_sustained": 1396.2,
+             "source": "test"}
+    r = bench.roofline_object(cfg.dtype, flops, fwd_bytes, 0.1, peaks, None)
+    assert r["bound"] == bound
+    want = flops / 1e-4 / 1e12 if bound == "tensor" else fwd_bytes / 1e-4 / 1e9
+    assert abs(r["achieved"] - want) <= 1e-9 * want
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-12
