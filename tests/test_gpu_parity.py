@@ -483,13 +483,11 @@ def test_forward_ex_rejects_bad_epilogue_arguments(sc):
     m.free()
 
 
-def test_decoder_scale_config():
+def test_decoder_scale_config(sc):
     """1024^3, 3.26M voxels, C=64 fp16 (the decoder-scale workload): the whole
     neighbour map bit-exact, outputs on sampled rows (first tile, ragged last
     tile, 3,000 random rows) within the half-precision bars."""
-    import sparse_voxel_convolution_coord_b300 as scm
-    if not torch.cuda.is_available():
-        pytest.skip("no CUDA device")
+    scm = sc
     p = synth.make_problem(6)
     m, nbr = gpu_map(scm, p.coords, p.res)
     want = oracle.build_neighbor_table(p.coords, p.res)
