@@ -19,6 +19,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -97,7 +98,9 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % gpu_index)
+        # raw samples in a scratch file; the line carries their summary
+        self.path = os.path.join(tempfile.gettempdir(),
+                                 "sc_bench_clocks_%d_rank%d.csv" % (os.getpid(), gpu_index))
 
     def start(self):
         try:
