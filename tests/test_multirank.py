@@ -100,3 +100,34 @@ def test_roofline_takes_the_binding_limit(key, bound):
     want = flops / 1e-4 / 1e12 if bound == "tensor" else fwd_bytes / 1e-4 / 1e9
     assert abs(r["achieved"] - want) <= 1e-9 * want
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-12
+
+
+def test_clock_sampler_summary_and_cleanup(tmp_path):
+    """The clock record's parsing: median SM clock, max clock, throttle
+    reasons that were active, and the scratch file removed afterwards."""
+    import os
+    import bench
+
+    class FakeProc:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+        def kill(self):
+            pass
+
+    cs = bench.ClockSampler(0)
+    cs.path = str(tmp_path / "clocks.csv")
+    rows = ["0, 2032, 2032, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "0, 2000, 2032, 950.0, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, 2032, 2032, 980.0, 0x0, Not Active, Not Active, Not Active, Not Active"]
+    with open(cs.path, "w") as f:
+        f.write("\n".join(rows) + "\n")
+    cs.f = open(os.devnull, "w")
+    cs.proc = FakeProc()
+    out = cs.stop()
+    assert out["sm_mhz"] == 2032 and out["sm_max_mhz"] == 2032 and out["samples"] == 3
+    assert out["reasons"] == ["sw_power_cap"]
+    assert not os.path.exists(cs.path)
