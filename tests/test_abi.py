@@ -81,3 +81,33 @@ def test_no_cpu_fallback_in_binding():
     import inspect
     src = inspect.getsource(sc)
     assert "oracle" not in src.replace("no CPU fallback", "")
+
+
+def test_header_is_plain_c(lib, tmp_path):
+    """include/sc.h compiles as C99 and a C program links against libsc.so
+    (no C++ in the ABI's declarations)."""
+    import os
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = tmp_path / "use_sc.c"
+    src.write_text(
+        '#include "sc.h"\n'
+        "#include <stdio.h>\n"
+        "int main(void) {\n"
+        "  sc_handle h = sc_build_map(0, -1, 4, 0);\n"
+        "  sc_activation a = SC_ACT_SILU;\n"
+        "  sc_dtype d = SC_F16;\n"
+        "  printf(\"%d %d %d %s\\n\", h == 0, (int)a, (int)d, sc_version());\n"
+        "  return sc_last_error() == SC_ERR_INVALID_ARG ? 0 : 1;\n"
+        "}\n")
+    exe = tmp_path / "use_sc"
+    libdir = os.path.dirname(sc.library_path())
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(root, "include"),
+                    str(src), "-o", str(exe), "-L", libdir, "-lsc",
+                    "-Wl,-rpath," + libdir], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.startswith("1 2 2 ")
