@@ -183,6 +183,17 @@ SC_API sc_status sc_set_deterministic(int32_t enable);
  */
 SC_API uint64_t sc_kernel_launches(void);
 
+/*
+ * Return to the device the memory the library keeps cached for later maps.
+ * Map buffers come from a library-owned stream-ordered pool that keeps freed
+ * memory reserved, since unmapping and remapping it costs more than a build.
+ * Live maps' memory is untouched, and so is memory whose stream-ordered free
+ * has not executed yet; synchronise those streams first to release
+ * everything.  Does nothing when sc_set_allocator routes allocations
+ * elsewhere.  SC_OK, or SC_ERR_CUDA.
+ */
+SC_API sc_status sc_release_cached_memory(void);
+
 /* Number of rows n of the map, or -1 (and SC_ERR_BAD_HANDLE) for a dead handle. */
 SC_API int64_t sc_map_size(sc_handle h);
 

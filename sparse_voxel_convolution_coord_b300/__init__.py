@@ -21,7 +21,7 @@ __all__ = [
     "ScError", "Map", "load_library", "library_path", "header_symbols",
     "sc_build_map", "sc_forward", "sc_free_map", "sc_map_size", "sc_map_pairs",
     "sc_get_neighbor_table", "sc_get_pairs", "sc_device_status", "sc_last_error",
-    "sc_last_error_msg", "sc_version", "sc_set_deterministic", "sc_kernel_launches", "SC_OK", "SC_ERR_INVALID_ARG", "SC_ERR_COORD_RANGE",
+    "sc_last_error_msg", "sc_version", "sc_set_deterministic", "sc_kernel_launches", "sc_release_cached_memory", "SC_OK", "SC_ERR_INVALID_ARG", "SC_ERR_COORD_RANGE",
     "SC_ERR_DUPLICATE", "SC_ERR_TABLE_FULL", "SC_ERR_UNSUPPORTED", "SC_ERR_ALLOC",
     "SC_ERR_CUDA", "SC_ERR_BAD_HANDLE", "SC_ERR_DEVICE_TIMEOUT", "SC_F32", "SC_BF16", "SC_F16",
     "SC_ACT_NONE", "SC_ACT_RELU", "SC_ACT_SILU", "sc_forward_ex",
@@ -93,6 +93,7 @@ def load_library():
     lib.sc_set_deterministic.argtypes = [I32]
     lib.sc_set_deterministic.restype = ctypes.c_int
     lib.sc_kernel_launches.restype = ctypes.c_uint64
+    lib.sc_release_cached_memory.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -112,6 +113,11 @@ def sc_version() -> str:
 def sc_kernel_launches() -> int:
     """Kernels the library has launched in this process (see sc.h)."""
     return int(load_library().sc_kernel_launches())
+
+
+def sc_release_cached_memory() -> None:
+    """Return the library pool's cached (freed) map memory to the device."""
+    _check(load_library().sc_release_cached_memory())
 
 
 def sc_set_deterministic(enable: bool) -> None:

@@ -171,6 +171,16 @@ sc_status sc_set_allocator(void* (*alloc)(size_t, void*, void*),
 
 uint64_t sc_kernel_launches(void) { return sc::launches(); }
 
+sc_status sc_release_cached_memory(void) {
+  std::lock_guard<std::mutex> lk(g_pool_mu);
+  for (int d = 0; d < kMaxPoolDevices; ++d) {
+    if (!g_pools[d]) continue;
+    const cudaError_t e = cudaMemPoolTrimTo(g_pools[d], 0);
+    if (e != cudaSuccess) return fail_cuda(e, "sc_release_cached_memory");
+  }
+  return ok();
+}
+
 sc_status sc_set_deterministic(int32_t enable) {
   if (enable != 0 && enable != 1)
     return fail(SC_ERR_INVALID_ARG, "sc_set_deterministic: enable must be 0 or 1");

@@ -14,6 +14,8 @@
 // offset ahead, and shared by the 8 warps.  Each output row is written once,
 // no atomics, through the fused epilogue (activation, residual, fp32, bf16 or
 // fp16 output).
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -139,12 +141,19 @@ template <int J>
 cudaError_t launch_simt(const sc_map* m, const float* feats, const float* w, const Epilogue& ep,
                         int cin, int cout, cudaStream_t s) {
   const size_t smem = 2ull * 32 * 32 * J * sizeof(float);
-  static bool attr = false;  // opt-in above 48 KB of dynamic shared memory
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_conv_simt_f32<J>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // Opt-in above 48 KB of dynamic shared memory, once per device (function
+  // attributes are per device; setting one twice is harmless).
+  constexpr int kMaxDevices = 64;
+  static std::atomic<bool> attr_set[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(k_conv_simt_f32<J>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
     if (e != cudaSuccess) return e;
-    attr = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   const unsigned blocks = (unsigned)((m->n + kSimtWarps - 1) / kSimtWarps);
   k_conv_simt_f32<J><<<blocks, kSimtWarps * 32, smem, s>>>(m->nbr, m->n, feats, w, ep, cin, cout);

@@ -31,6 +31,11 @@ def test_deterministic_switch_checks_its_argument(lib):
     assert lib.sc_set_deterministic(0) == sc.SC_OK
 
 
+def test_release_cached_memory_without_pools(lib):
+    # no map built in this process: no pool exists, nothing to trim
+    assert lib.sc_release_cached_memory() == sc.SC_OK
+
+
 def test_launch_counter_is_exported(lib):
     assert sc.sc_kernel_launches() >= 0
 

@@ -503,3 +503,16 @@ def test_decoder_scale_config(sc):
     m.free()
     ref = oracle.conv(want[rows], p.feats, p.weight, p.bias)
     assert_close(got, ref, "f16", "config 6")
+
+
+def test_release_cached_memory_then_rebuild(sc):
+    """Trimming the library's pool after a map is freed (and its stream has
+    run the free) leaves later builds working."""
+    p = synth.make_problem(2)
+    m, nbr = gpu_map(sc, p.coords, p.res)
+    m.free()
+    torch.cuda.synchronize()
+    sc.sc_release_cached_memory()
+    m2, nbr2 = gpu_map(sc, p.coords, p.res)
+    np.testing.assert_array_equal(nbr, nbr2)
+    m2.free()
