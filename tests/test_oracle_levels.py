@@ -217,3 +217,25 @@ def test_planted_level_mistakes_are_caught(name):
         except (AssertionError, IndexError, ValueError):
             failed.append(check.__name__)
     assert failed, "no pin caught %s" % name
+
+
+def test_golden_levels():
+    import json
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "levels",
+                        "one_voxel_three_children.json")
+    g = json.load(open(path))
+    child, parent, offset = levels.subdivide(np.array(g["coords"]), np.array(g["mask"]))
+    np.testing.assert_array_equal(child, g["children"])
+    np.testing.assert_array_equal(parent, g["parent"])
+    np.testing.assert_array_equal(offset, g["offset"])
+    feats = np.arange(16, dtype=np.float64)[None, :]
+    np.testing.assert_array_equal(levels.channel_to_spatial(feats, parent, offset), g["c2s_out"])
+    par, child_of, _ = levels.downsample_map(np.array(g["children"]))
+    np.testing.assert_array_equal(par, g["parents_down"])
+    np.testing.assert_array_equal(child_of, g["child_of"])
+    w = np.stack([(o + 1) * np.eye(2) for o in range(8)])
+    up = levels.conv_up(parent, offset, np.array(g["parent_feats"]), w, np.array(g["bias"]))
+    np.testing.assert_array_equal(up, g["up_out"])
+    down = levels.conv_down(child_of, np.array(g["child_feats"]), w, np.array(g["bias"]))
+    np.testing.assert_array_equal(down, g["down_out"])

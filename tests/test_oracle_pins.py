@@ -470,3 +470,11 @@ def test_planted_epilogue_mistakes_are_caught(name):
             except AssertionError:
                 failed += 1
     assert failed, "no epilogue pin caught %s" % name
+
+
+def test_golden_epilogue():
+    g = json.load(open(os.path.join(GOLDEN, "epilogue", "relu_residual_bf16.json")))
+    acts = {"none": oracle.ACT_NONE, "relu": oracle.ACT_RELU, "silu": oracle.ACT_SILU}
+    y = oracle.epilogue(np.array(g["conv_out"]), acts[g["act"]], np.array(g["residual"]))
+    np.testing.assert_allclose(y, np.array(g["out_f32"]), rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(oracle.round_bf16(y), np.array(g["out_bf16"]))
