@@ -749,7 +749,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 namespace {
 
-// The driver's tensor-map encoder, looked up once (thread-safe static init).
+// cuTensorMapEncodeTiled from the CUDA driver API, looked up once
+// (thread-safe static initialisation).
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* ptr = nullptr;
