@@ -149,6 +149,19 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU oracle legs (the only places bench.py runs oracle/)
 
+def cpu_model():
+    """The host CPU's model name (from /proc/cpuinfo), or the platform's."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or "unknown"
+
+
 def oracle_sample_run(p, rows, threads=0):
     """Oracle map build over all voxels + fp64 convolution of `rows`."""
     import oracle
@@ -205,7 +218,7 @@ def cpu_baseline(p, target_s=20.0, single_s=4.0):
     rows1 = np.sort(rng.choice(p.n, size=m1, replace=False))
     dt1, pairs1 = oracle_sample_run(p, rows1, threads=1)
     return {"value": tflops, "unit": "TFLOP/s", "cores": oracle.max_threads(),
-            "kind": "oracle",
+            "kind": "oracle", "cpu_model": cpu_model(), "nproc": os.cpu_count(),
             "sample": "%s: %d pairs in %.1f s; voxels/s %.3g" % (what, pairs, dt, rows_done / dt),
             "single_thread": {
                 "value": 2.0 * pairs1 * cin * cout / dt1 / 1e12, "unit": "TFLOP/s", "cores": 1,

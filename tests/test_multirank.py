@@ -77,6 +77,7 @@ def test_cpu_baseline_reports_all_cores_and_one_thread():
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1
     assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
     assert "whole workload" in cb["sample"] or "sampled" in cb["sample"]
+    assert cb["cpu_model"] and cb["nproc"] >= 1
 
 
 @pytest.mark.parametrize("key,bound", [(3, "tensor"), (5, "hbm"), (1, "hbm")])
