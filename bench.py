@@ -10,8 +10,11 @@ present (output, neighbour) pairs only) and active voxels/s.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 3]
     python bench.py --impl reference ...   # the CPU oracle, on host cores
 
-Multi-GPU: replicas only (each rank runs the same workload on its own GPU,
-no collective on the data path); value = units of all ranks / max time.
+One GPU only: the path does not shard (replicas at most), and the tensor-core
+convolution shares its weight slices between the two CTAs of a cluster by TMA
+multicast, which is kept to single-GPU runs.  With --gpus N > 1, or under a
+launcher with WORLD_SIZE > 1, our arm prints one "unavailable" line (rank 0)
+and exits 0.  The reference arm (the CPU oracle) runs on rank 0 alone.
 """
 import argparse
 import json
@@ -40,6 +43,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = same as --steps (max 500)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-map-gate", action="store_true",
+                    help="skip timing the 256^3 ~400k-voxel map build beside the workload")
     return ap.parse_args()
 
 
@@ -50,33 +55,15 @@ def dist_env():
     return rank, world, local
 
 
-def init_dist(world):
-    if world <= 1:
-        return None
-    import torch.distributed as dist
-    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-    dist.init_process_group("gloo")
-    return dist
+MULTI_GPU_UNAVAILABLE = (
+    "multi-GPU runs are not made: the path runs on one GPU (replicas only, no data-path "
+    "exchange), and k_conv_tc multicasts W slices between the two CTAs of a cluster "
+    "(cp.async.bulk.tensor .multicast::cluster), which is kept to single-GPU runs")
 
 
-def max_over_ranks(dist, v):
-    if dist is None:
-        return v
-    import torch
-    t = torch.tensor([float(v)], dtype=torch.float64)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def barrier(dist):
-    if dist is not None:
-        dist.barrier()
-
-
-def whole_job_rate(world, units_per_rank, t_max_ms):
-    """Weak scaling, replicas: every rank processes units_per_rank in its step;
-    the job's rate is all ranks' units over the slowest rank's step time."""
-    return world * units_per_rank / (t_max_ms * 1e-3)
+def multi_gpu_line(n_gpus):
+    """The line our arm prints instead of running on more than one GPU."""
+    return {"metric": METRIC, "n_gpus": n_gpus, "unavailable": MULTI_GPU_UNAVAILABLE}
 
 
 def load_peaks():
@@ -102,10 +89,25 @@ class ClockSampler:
         self.path = os.path.join(tempfile.gettempdir(),
                                  "sc_bench_clocks_%d_rank%d.csv" % (os.getpid(), gpu_index))
 
+    def one_shot(self):
+        """One synchronous query, appended to the record (a timed region
+        shorter than the sampling period still gets a sample on each side)."""
+        try:
+            r = subprocess.run(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
+                                "--format=csv,noheader,nounits"], capture_output=True,
+                               text=True, timeout=10)
+            if r.returncode == 0 and r.stdout.strip():
+                with open(self.path, "a") as f:
+                    f.write(r.stdout.strip() + "\n")
+        except Exception:
+            pass
+
     def start(self):
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
+            open(self.path, "w").close()
+            self.one_shot()
+            self.f = open(self.path, "a")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
                  "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
@@ -122,6 +124,7 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
+        self.one_shot()
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
@@ -333,10 +336,59 @@ def roofline_object(dtype, flops, fwd_bytes, t_kernel_ms, peaks, traffic):
             "tensor_tflops": flops / t_s / 1e12, "algorithmic_bytes_per_launch": fwd_bytes}
 
 
+def time_build(sc, torch, coords, res, flush, stream, reps=60):
+    """Map build timed two ways on the same coordinates, L2 flushed before each:
+    device-only (CUDA events around sc_build_map_async: init, insert and query
+    kernels, with the stream held by a GPU sleep so host gaps do not count)
+    and host-inclusive (host time of sc_build_map, which synchronises once to
+    read the status and pair count).  Returns medians in ms."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    maps = []
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(2e7))
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        maps.append(sc.sc_build_map_async(coords, res, 1))
+        e1.record(stream)
+    torch.cuda.synchronize()
+    sc.sc_map_status(maps[-1])
+    for m in maps:
+        m.free()
+    dev_ms = statistics.median(a.elapsed_time(b) for a, b in evs[5:])
+    host = []
+    for _ in range(reps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        m = sc.sc_build_map(coords, res)
+        host.append((time.perf_counter() - t0) * 1e3)
+        m.free()
+    torch.cuda.synchronize()
+    return dev_ms, statistics.median(host[5:])
+
+
+def map_build_object(n, dev_ms, host_ms, peaks, what):
+    """The map build against its algorithmic bytes (coords 16N + one slot write
+    8N + neighbour table 108N)."""
+    b = 132 * n
+    return {"workload": what, "bound": "hbm", "n_voxels": n, "algorithmic_bytes": b,
+            "device_us": dev_ms * 1e3, "achieved_gbs": b / (dev_ms * 1e-3) / 1e9,
+            "frac_of_hbm": b / (dev_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "host_inclusive_us": host_ms * 1e3,
+            "achieved_gbs_host_inclusive": b / (host_ms * 1e-3) / 1e9,
+            "frac_of_hbm_host_inclusive": b / (host_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "peak_source": peaks["source"] + " hbm"}
+
+
 def run_ours(args):
-    import torch
     rank, world, local = dist_env()
-    dist = init_dist(world)
+    if args.gpus > 1 or world > 1:
+        if rank == 0:
+            print(json.dumps(multi_gpu_line(max(args.gpus, world))), flush=True)
+        return
+    import torch
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     import sparse_voxel_convolution_coord_b300 as sc
@@ -346,6 +398,7 @@ def run_ours(args):
 
     p = synth.make_problem(args.config)
     cin, cout = p.feats.shape[1], p.weight.shape[2]
+    nbatch = int(p.coords[:, 0].max()) + 1 if p.n else 1
     tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[p.config.dtype]
     esize = 4 if p.config.dtype == "f32" else 2
     coords = torch.from_numpy(p.coords).to(dev)
@@ -362,48 +415,50 @@ def run_ours(args):
     flops = 2.0 * pairs * cin * cout
     # algorithmic bytes (every byte the path must move once)
     fwd_bytes = p.n * cin * esize + 108 * p.n + 4 * p.n * cout + 27 * cin * cout * esize
-    build_bytes = 132 * p.n  # coords 16N + one slot write 8N + neighbour table 108N
 
-    # -- the timed step: map build + forward, L2 flushed before each step
+    # -- the timed step: map build (asynchronous: no host synchronisation) +
+    # forward, L2 flushed before each step outside the events
     def step(evs=None):
         if evs is not None:
             evs[0].record(stream)
-        mp = sc.sc_build_map(coords, p.res)
+        mp = sc.sc_build_map_async(coords, p.res, nbatch)
         if evs is not None:
             evs[1].record(stream)
         sc.sc_forward(mp, feats, weight, bias, out)
         if evs is not None:
             evs[2].record(stream)
-        mp.free()
+        return mp
 
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
-        step()
+        step().free()
     torch.cuda.synchronize()
 
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     clocks = ClockSampler(local)
     clocks.start()
-    barrier(dist)
     torch.cuda.synchronize()
     launches0 = sc.sc_kernel_launches()
     wall0 = time.perf_counter()
     for i in range(K):
         flush.zero_()
-        step(evs[i])
+        step(evs[i]).free()
     torch.cuda.synchronize()
-    barrier(dist)
     wall = time.perf_counter() - wall0
     gpu_launches = sc.sc_kernel_launches() - launches0
     clk = clocks.stop()
+    # the timed builds ran on the same coordinates: one more must report no error
+    mp = step()
+    sc.sc_map_status(mp)
+    sc.sc_device_status(mp)
+    mp.free()
     step_ms = [e[0].elapsed_time(e[2]) for e in evs]
     build_ms = [e[0].elapsed_time(e[1]) for e in evs]
     fwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
     t_step = sum(step_ms) / K
     t_build = sum(build_ms) / K
     t_fwd = sum(fwd_ms) / K
-    t_step_max = max_over_ranks(dist, t_step)
 
     # -- the convolution kernel alone (roofline), on one map
     mp = sc.sc_build_map(coords, p.res)
@@ -412,6 +467,19 @@ def run_ours(args):
     t_kernel = time_forward_alone(sc, torch, mp, feats, weight, bias, out, flush, stream)
     sc.sc_device_status(mp)
     mp.free()
+
+    # -- the map build alone: this workload, and the 256^3 ~400k-voxel shells
+    # (the largest single build, where the HBM target is set)
+    peaks = load_peaks()
+    dev_b, host_b = time_build(sc, torch, coords, p.res, flush, stream)
+    map_build = map_build_object(p.n, dev_b, host_b, peaks, p.config.name)
+    gate = None
+    if args.config != 5 and not args.no_map_gate:
+        p5 = synth.make_problem(5)
+        c5 = torch.from_numpy(p5.coords).to(dev)
+        dev5, host5 = time_build(sc, torch, c5, p5.res, flush, stream)
+        gate = map_build_object(p5.n, dev5, host5, peaks, p5.config.name)
+        del c5
 
     # -- end to end through the public API from pinned host buffers
     h_coords = torch.from_numpy(p.coords).pin_memory()
@@ -431,7 +499,7 @@ def run_ours(args):
         d_feats.copy_(h_feats, non_blocking=True)
         d_weight.copy_(h_weight, non_blocking=True)
         d_bias.copy_(h_bias, non_blocking=True)
-        mp = sc.sc_build_map(d_coords, p.res)
+        mp = sc.sc_build_map_async(d_coords, p.res, nbatch)
         sc.sc_forward(mp, d_feats, d_weight, d_bias, out)
         h_out.copy_(out, non_blocking=True)
         mp.free()
@@ -442,45 +510,43 @@ def run_ours(args):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    barrier(dist)
     e0.record(stream)
     for _ in range(KE):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    t_e2e = max_over_ranks(dist, e0.elapsed_time(e1) / KE)
+    t_e2e = e0.elapsed_time(e1) / KE
 
-    peaks = load_peaks()
     conv_src = os.path.join(ROOT, "sparse_voxel_convolution_coord_b300", "csrc", "sc_conv_tc.cu")
     traffic = None
     rec = MEASURED_TRAFFIC.get(p.config.name)
     if rec is not None and p.config.dtype != "f32" and rec[0] == _file_sha1(conv_src):
         traffic = rec[1]
     roofline = roofline_object(p.config.dtype, flops, fwd_bytes, t_kernel, peaks, traffic)
-    build_gbs = build_bytes / (t_build * 1e-3) / 1e9
     line = {
         "metric": METRIC,
-        "value": whole_job_rate(world, flops, t_step_max) / 1e12,
+        "value": flops / (t_step * 1e-3) / 1e12,
         "unit": "TFLOP/s",
-        "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": t_step_max,
+        "n_gpus": 1, "steps": K, "warmup": args.warmup,
+        "ms_per_step": t_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": p.config.dtype,
         "data": "synthetic (seeded superquadric voxel shells; random N(0,1) features, "
                 "N(0, 1/sqrt(27 cin)) weights)",
         "config": {"workload": p.config.name, "description": p.config.description,
                    "n_voxels": p.n, "pairs": pairs, "cin": cin, "cout": cout, "res": p.res,
-                   "parallelism": "replicas" if world > 1 else "single",
+                   "parallelism": "single",
+                   "step": "sc_build_map_async (hash + neighbour map, no host sync) + "
+                           "sc_forward (gather-GEMM + bias); build errors checked after",
                    "l2": "flushed before every timed step (256 MB write, outside the events)"},
-        "voxels_per_s": whole_job_rate(world, p.n, t_step_max),
-        "breakdown_ms": {"build_map_incl_host_sync": t_build, "forward_in_step": t_fwd,
+        "voxels_per_s": p.n / (t_step * 1e-3),
+        "breakdown_ms": {"build_map_in_step": t_build, "forward_in_step": t_fwd,
                          "forward_kernel_alone": t_kernel,
                          "wall_per_step_incl_flush": wall / K * 1e3},
         "roofline": roofline,
-        "map_build": {"bound": "hbm", "algorithmic_bytes": build_bytes,
-                      "achieved_gbs_incl_host_sync": build_gbs,
-                      "frac_of_hbm": build_gbs / peaks["hbm_gbs"]},
-        "e2e": {"value": whole_job_rate(world, flops, t_e2e) / 1e12, "unit": "TFLOP/s",
+        "map_build": map_build,
+        "map_build_256cubed_400k": gate,
+        "e2e": {"value": flops / (t_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": t_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         # counted by the library at each of its launches over the timed steps
         # (map build: init, insert, query; forward: conv, plus the zeroing
@@ -488,12 +554,9 @@ def run_ours(args):
         "gpu_launches": gpu_launches,
         "clocks": clk,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.destroy_process_group()
+    print(json.dumps(line), flush=True)
 
 
 def main():

@@ -53,8 +53,9 @@ typedef enum {
   SC_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, bad alignment, ... */
   SC_ERR_COORD_RANGE = 2,  /* a coordinate outside [0,res) or a negative batch  */
   SC_ERR_DUPLICATE = 3,    /* two rows with the same (b,x,y,z)                  */
-  SC_ERR_TABLE_FULL = 4,   /* hash probe bound exceeded (cannot happen: the
-                              table's load factor is at most 1/2)               */
+  SC_ERR_TABLE_FULL = 4,   /* hash probe bound exceeded (at the table's load
+                              factor of at most 1/2 only under a probe limit
+                              set by sc_set_probe_limit)                        */
   SC_ERR_UNSUPPORTED = 5,  /* shape/dtype outside the kernels' envelope         */
   SC_ERR_ALLOC = 6,        /* device allocation failed                          */
   SC_ERR_CUDA = 7,         /* a CUDA runtime/driver call failed                 */
@@ -103,6 +104,39 @@ typedef enum {
 SC_API sc_handle sc_build_map(const int32_t* coords, int64_t n, int32_t res, void* stream);
 
 /*
+ * sc_build_map without any host synchronisation: the hash build and the
+ * neighbour map are enqueued on `stream` and the handle is returned at once,
+ * so that the build overlaps host work and the convolutions enqueued after
+ * it (same definition and citations as sc_build_map).
+ *
+ *   nbatch  batch indices must lie in [0, nbatch), nbatch >= 1.  It fixes the
+ *           hash key width up front (32-bit keys when nbatch * res^3 < 2^32),
+ *           so there is no retry; SC_ERR_UNSUPPORTED when even 64-bit keys
+ *           cannot hold nbatch * res^3 (see sc_build_map).
+ * The map's buffers are ready in stream order on `stream`: sc_forward on the
+ * same stream (or one ordered after it) can follow at once.  Errors the
+ * device finds (a coordinate outside [0,res), a batch index outside
+ * [0,nbatch), duplicate rows) are not returned here: the first call that
+ * needs the build's result -- sc_map_status, sc_map_pairs, sc_device_status
+ * -- waits for the build and reports them (SC_ERR_COORD_RANGE,
+ * SC_ERR_DUPLICATE, SC_ERR_TABLE_FULL), and they stay with the map.  A
+ * convolution over a map whose build failed computes garbage but never
+ * reads or writes outside its buffers.  Returns NULL only for errors found
+ * on the host (SC_ERR_INVALID_ARG, SC_ERR_UNSUPPORTED, SC_ERR_ALLOC,
+ * SC_ERR_CUDA).  No counterpart on the pages beyond sc_build_map's.
+ */
+SC_API sc_handle sc_build_map_async(const int32_t* coords, int64_t n, int32_t res, int32_t nbatch,
+                                    void* stream);
+
+/*
+ * Wait for the map's build (if sc_build_map_async left it unread) and return
+ * its outcome: SC_OK or the build's error (see above).  Synchronises with
+ * the build only, not with later work on its stream.  Error plumbing with no
+ * counterpart on the pages.
+ */
+SC_API sc_status sc_map_status(sc_handle h);
+
+/*
  * Run the convolution over a built map: for each output row o (input order)
  *   out[o][:] = bias[:] + sum_k feats[nbr[o][k]][:] @ W[k]   (k with nbr >= 0)
  * ("Porting TRELLIS.2 ...", section V: gather-GEMM over the neighbour table,
@@ -119,6 +153,13 @@ SC_API sc_handle sc_build_map(const int32_t* coords, int64_t n, int32_t res, voi
  *   weight  device [27][cin][cout], dtype `dtype`, row-major, 16-byte aligned.
  *   bias    device fp32 [cout], or NULL for zero bias.
  *   out     device fp32 [n][cout], row-major, 16-byte aligned; fully written.
+ *           It must not overlap feats, weight or bias.
+ * Every pointer must be ordinary device memory of the map's device
+ * (cudaMalloc, a stream-ordered pool or a VMM mapping); host memory (even
+ * pinned or mapped), managed memory and another GPU's memory give
+ * SC_ERR_INVALID_ARG before anything is launched.  (The tensor-core kernel
+ * reads W through a tensor map whose loads are shared by the two CTAs of a
+ * cluster on this GPU.)
  *   dtype   SC_BF16 / SC_F16: tensor-core path (tcgen05, bf16 x bf16 or
  *           fp16 x fp16 -> fp32 in TMEM); cin in {16, 32} or a multiple of
  *           64 up to 1024; cout a multiple of 16 up to 256.
@@ -140,7 +181,10 @@ SC_API sc_status sc_forward(sc_handle h, const void* feats, const void* weight, 
  * neither the activation nor the order; the activation is applied to the
  * convolution's output and the residual (a skip connection) added after it.
  *
- *   residual  device [n][cout] in out_dtype, 16-byte aligned, or NULL.
+ *   residual  device [n][cout] in out_dtype, 16-byte aligned, or NULL.  It
+ *             may be out itself (an in-place skip connection: each element
+ *             is read before it is written); any other overlap with out is
+ *             SC_ERR_INVALID_ARG.
  *   out       device [n][cout] in out_dtype, 16-byte aligned; fully written.
  *   act       SC_ACT_NONE, SC_ACT_RELU or SC_ACT_SILU.
  *   out_dtype SC_F32, SC_BF16 or SC_F16 (any with any input dtype); bf16
@@ -148,9 +192,12 @@ SC_API sc_status sc_forward(sc_handle h, const void* feats, const void* weight, 
  *             to infinity past 65,504).
  * sc_forward(...) is sc_forward_ex(..., NULL residual, SC_ACT_NONE, SC_F32).
  * On the tensor-core path an activation or a 16-bit output turns the tail split
- * (see sc_forward) off, since neither can be applied to a partial sum; a
- * residual alone keeps it (the last part adds it).
- * Errors as sc_forward, plus SC_ERR_INVALID_ARG for a bad act or out_dtype.
+ * (see sc_forward) off, since neither can be applied to a partial sum; so
+ * does residual == out, since the split rows are zeroed and summed into
+ * before the last part would read the residual from them.  A separate
+ * residual keeps the split (the last part adds it).
+ * Errors as sc_forward, plus SC_ERR_INVALID_ARG for a bad act or out_dtype
+ * or a residual that partly overlaps out.
  */
 SC_API sc_status sc_forward_ex(sc_handle h, const void* feats, const void* weight,
                                const float* bias, const void* residual, void* out, int32_t cin,
@@ -158,7 +205,8 @@ SC_API sc_status sc_forward_ex(sc_handle h, const void* feats, const void* weigh
                                void* stream);
 
 /*
- * Release a map.  Its device memory is freed in stream order on `stream`:
+ * Release a map (library plumbing: the pages have no counterpart; they keep
+ * maps in a per-tensor cache).  Its device memory is freed in stream order on `stream`:
  * the caller must order every other stream that used the map before that
  * stream.  A handle that is not live (freed already, or never returned by
  * sc_build_map) gives SC_ERR_BAD_HANDLE and is not touched.  NULL is a no-op.
@@ -166,7 +214,9 @@ SC_API sc_status sc_forward_ex(sc_handle h, const void* feats, const void* weigh
 SC_API sc_status sc_free_map(sc_handle h, void* stream);
 
 /*
- * Deterministic mode for sc_forward (process-wide; default 0).  With 1, every
+ * Deterministic mode for sc_forward (process-wide; default 0; no counterpart
+ * on the pages, whose reference layer is compared bit for bit against one
+ * run of their own kernel).  With 1, every
  * call on the same inputs returns bit-identical outputs, at the cost of the
  * tail split described under sc_forward (a last partial round of tiles then
  * runs as fewer, longer parts).  Returns SC_OK, or SC_ERR_INVALID_ARG for a
@@ -175,6 +225,7 @@ SC_API sc_status sc_free_map(sc_handle h, void* stream);
 SC_API sc_status sc_set_deterministic(int32_t enable);
 
 /*
+ * Instrumentation with no counterpart on the pages.
  * Number of GPU kernels this library has launched in this process, counted on
  * the host at each launch (map build: 3 per sc_build_map, 6 when it retries
  * with 64-bit keys; sc_forward: 1, or 2 when the tensor-core path zeroes
@@ -184,6 +235,7 @@ SC_API sc_status sc_set_deterministic(int32_t enable);
 SC_API uint64_t sc_kernel_launches(void);
 
 /*
+ * Memory plumbing with no counterpart on the pages.
  * Return to the device the memory the library keeps cached for later maps.
  * Map buffers come from a library-owned stream-ordered pool that keeps freed
  * memory reserved, since unmapping and remapping it costs more than a build.
@@ -194,10 +246,15 @@ SC_API uint64_t sc_kernel_launches(void);
  */
 SC_API sc_status sc_release_cached_memory(void);
 
-/* Number of rows n of the map, or -1 (and SC_ERR_BAD_HANDLE) for a dead handle. */
+/* Number of rows n of the map, or -1 (and SC_ERR_BAD_HANDLE) for a dead handle
+ * (an accessor with no counterpart on the pages). */
 SC_API int64_t sc_map_size(sc_handle h);
 
-/* Total pair count P = sum_k |{o : nbr[o][k] >= 0}|, or -1 for a dead handle. */
+/* Total pair count P = sum_k |{o : nbr[o][k] >= 0}|, or -1 for a dead handle
+ * or a failed asynchronous build (whose build it waits for first):
+ * the number of (input, output) pairs that "Running TRELLIS.2 on a Mac (1/3)",
+ * Sparse 3D convolution, gathers and multiplies, which sets the layer's
+ * effective work 2 * P * cin * cout. */
 SC_API int64_t sc_map_pairs(sc_handle h);
 
 /*
@@ -218,6 +275,7 @@ SC_API sc_status sc_get_neighbor_table(sc_handle h, int32_t* nbr_out, void* stre
 SC_API sc_status sc_get_pairs(sc_handle h, int64_t* off_host, int32_t* in, int32_t* out, void* stream);
 
 /*
+ * Allocation plumbing with no counterpart on the pages.
  * Install a device allocator for the map's buffers (e.g. a framework's
  * caching allocator).  alloc(bytes, stream, ctx) returns a device pointer or
  * NULL; free(ptr, stream, ctx) releases it in stream order.  Passing NULL for
@@ -228,9 +286,12 @@ SC_API sc_status sc_set_allocator(void* (*alloc)(size_t bytes, void* stream, voi
                            void (*free_fn)(void* ptr, void* stream, void* ctx), void* ctx);
 
 /*
+ * Error plumbing with no counterpart on the pages.
  * Synchronise `stream` and report the map's device status word: SC_OK, or the
  * first error a bounded device loop of a kernel using this map recorded since
  * the last call (SC_ERR_DEVICE_TIMEOUT, SC_ERR_TABLE_FULL).  Clears the word.
+ * An asynchronous build's own error (see sc_build_map_async) is reported
+ * first, and on every call.
  */
 SC_API sc_status sc_device_status(sc_handle h, void* stream);
 
@@ -258,18 +319,133 @@ SC_API sc_status sc_device_status(sc_handle h, void* stream);
  * first call before any stream capture.  All calls share the one array and
  * each clears what it needs, so calls that overlap on the GPU (other streams,
  * other host threads) race and must be serialised by the caller.  The call
- * itself allocates nothing: no cudaMalloc, cudaFree or allocating library
- * routine.
+ * itself allocates nothing: no cudaMalloc, cudaFree, cudaHostAlloc or
+ * allocating library routine; the status words come back into a buffer on
+ * the calling thread's stack.
  */
 SC_API sc_status sc_build_neighbor_table_noalloc(const int32_t* coords, int64_t n, int32_t res,
                                                  int32_t* nbr_out, int64_t* pairs_out,
                                                  void* stream);
 
-/* Thread-local status and message of the last failing call on this thread. */
+/* ------------------------------------------------------------------------
+ * Level changes: moving a sparse voxel set between resolution levels.
+ * The trellis2mlx README names these operations -- its pipeline list's
+ * "Upsample" stage (the decoder's subdivision predictions become the
+ * high-resolution coordinates), its stage table (2,977 low-resolution voxels
+ * become 761,916) and its project layout (a sparse UNet decoder upsampling
+ * by Channel2Spatial) -- without fixing their details; the readings taken
+ * are stated at each call.
+ */
+typedef struct sc_level* sc_level_handle; /* opaque level map owned by the library */
+
+/*
+ * Children of each voxel whose mask bit is set: child o (0..7) of (b, x, y,
+ * z) is (b, 2x + (o >> 2 & 1), 2y + (o >> 1 & 1), 2z + (o & 1)) -- the same
+ * row-major flattening as the 27 offsets.  Children are listed parent by
+ * parent in input order, ascending o within a parent.
+ *   coords        device int32 [n][4] at resolution res, 16-byte aligned.
+ *   mask          device uint8 [n] (bit o: child o exists), or NULL for all 8.
+ *   n             0 <= n < 2^28;  res  1 <= res <= 2^19 (children at 2 res).
+ *   child_coords  device int32 [capacity][4], 16-byte aligned: room for every
+ *                 selected child (8n always suffices).
+ *   parent, offset  device int32 [capacity] or NULL: each child's parent row
+ *                 and o.
+ *   child_of      device int32 [n][8] or NULL: row of child o of each voxel,
+ *                 or -1.
+ *   m_out         host: receives the number of children M.
+ * Synchronises `stream` once (to return M).  SC_ERR_COORD_RANGE for a
+ * coordinate outside [0,res) or a negative batch, SC_ERR_INVALID_ARG,
+ * SC_ERR_ALLOC, SC_ERR_CUDA.
+ */
+SC_API sc_status sc_subdivide(const int32_t* coords, const uint8_t* mask, int64_t n, int32_t res,
+                              int32_t* child_coords, int32_t* parent, int32_t* offset,
+                              int32_t* child_of, int64_t* m_out, void* stream);
+
+/*
+ * Channel2Spatial: each child takes C of its parent's 8C channels, child o
+ * channel c = parent channel c * 8 + o (the sub-voxel index runs fastest, as
+ * in the dense pixel shuffle).
+ *   feats   device [n_parents][8c] in dtype.
+ *   parent, offset  device int32 [m] (as sc_subdivide returns them).
+ *   out     device [m][c] in dtype.
+ * Asynchronous on `stream`.
+ */
+SC_API sc_status sc_channel_to_spatial(const void* feats, const int32_t* parent,
+                                       const int32_t* offset, int64_t m, int32_t c, sc_dtype dtype,
+                                       void* out, void* stream);
+
+/*
+ * The way down: the parents of n voxels at resolution res are the distinct
+ * (b, x >> 1, y >> 1, z >> 1), listed in (b, x, y, z) order, each with the
+ * row of its child o (o as in sc_subdivide) or -1.  The returned map also
+ * drives the 2x2x2 stride-2 convolutions between the two levels.
+ *   coords  device int32 [n][4] (the fine voxels), 16-byte aligned.
+ *   res     1 <= res <= 2^20;  nbatch: batch indices lie in [0, nbatch).
+ * Synchronises `stream` once.  NULL with SC_ERR_COORD_RANGE (a coordinate
+ * outside [0,res) or a batch index outside [0,nbatch)), SC_ERR_DUPLICATE,
+ * SC_ERR_UNSUPPORTED (nbatch * ceil(res/2)^3 beyond 2^63), SC_ERR_INVALID_ARG,
+ * SC_ERR_ALLOC or SC_ERR_CUDA.
+ */
+SC_API sc_level_handle sc_build_level_map(const int32_t* coords, int64_t n, int32_t res,
+                                          int32_t nbatch, void* stream);
+
+/* Number of parents P, or -1 (SC_ERR_BAD_HANDLE) for a dead handle. */
+SC_API int64_t sc_level_parents(sc_level_handle h);
+
+/*
+ * Copy the map out (any output may be NULL): parent_coords device int32
+ * [P][4]; child_of device int32 [P][8] (row of child o, -1 if absent);
+ * parent_of device int32 [n] (each fine voxel's parent).  Asynchronous.
+ */
+SC_API sc_status sc_get_level_map(sc_level_handle h, int32_t* parent_coords, int32_t* child_of,
+                                  int32_t* parent_of, void* stream);
+
+/*
+ * 2x2x2 stride-2 convolution down a level, weights W[8][cin][cout] (the
+ * (Kvol, Ci, Co) layout with Kvol = 8, o as above):
+ *   out[p] = act(bias + sum_o feats[child_of[p][o]] @ W[o]) + residual[p]
+ * over present children; feats [n][cin] (fine rows), out [P][cout].  The
+ * epilogue, dtypes, shape envelope and pointer rules are those of
+ * sc_forward_ex.  Asynchronous on `stream`.
+ */
+SC_API sc_status sc_conv_down(sc_level_handle h, const void* feats, const void* weight,
+                              const float* bias, const void* residual, void* out, int32_t cin,
+                              int32_t cout, sc_dtype dtype, sc_activation act, sc_dtype out_dtype,
+                              void* stream);
+
+/*
+ * Its transpose, up a level:
+ *   out[i] = act(bias + feats[parent_of[i]] @ W[octant of i]) + residual[i]
+ * for every fine voxel i; feats [P][cin] (parent rows), out [n][cout].
+ * Otherwise as sc_conv_down.
+ */
+SC_API sc_status sc_conv_up(sc_level_handle h, const void* feats, const void* weight,
+                            const float* bias, const void* residual, void* out, int32_t cin,
+                            int32_t cout, sc_dtype dtype, sc_activation act, sc_dtype out_dtype,
+                            void* stream);
+
+/* As sc_device_status, for the convolutions over a level map. */
+SC_API sc_status sc_level_device_status(sc_level_handle h, void* stream);
+
+/* Release a level map (stream-ordered, as sc_free_map). */
+SC_API sc_status sc_free_level_map(sc_level_handle h, void* stream);
+
+/*
+ * Cap, for testing the hash's bounded probe loop, on the slots one key's
+ * insertion may probe (process-wide; 0, the default, = the table's
+ * capacity).  Builds whose insertion needs more probes fail with
+ * SC_ERR_TABLE_FULL (sc_build_map, sc_build_neighbor_table_noalloc).  With
+ * 1, any key whose home slot is taken by another key fails the build.  No
+ * counterpart on the pages.  SC_OK, or SC_ERR_INVALID_ARG for limit < 0.
+ */
+SC_API sc_status sc_set_probe_limit(int32_t limit);
+
+/* Thread-local status and message of the last failing call on this thread
+ * (error plumbing with no counterpart on the pages). */
 SC_API sc_status sc_last_error(void);
 SC_API const char* sc_last_error_msg(void);
 
-/* Library version string. */
+/* Library version string (no counterpart on the pages). */
 SC_API const char* sc_version(void);
 
 #ifdef __cplusplus

@@ -24,7 +24,11 @@ __all__ = [
     "sc_last_error_msg", "sc_version", "sc_set_deterministic", "sc_kernel_launches", "sc_release_cached_memory", "SC_OK", "SC_ERR_INVALID_ARG", "SC_ERR_COORD_RANGE",
     "SC_ERR_DUPLICATE", "SC_ERR_TABLE_FULL", "SC_ERR_UNSUPPORTED", "SC_ERR_ALLOC",
     "SC_ERR_CUDA", "SC_ERR_BAD_HANDLE", "SC_ERR_DEVICE_TIMEOUT", "SC_F32", "SC_BF16", "SC_F16",
-    "SC_ACT_NONE", "SC_ACT_RELU", "SC_ACT_SILU", "sc_forward_ex",
+    "SC_ACT_NONE", "SC_ACT_RELU", "SC_ACT_SILU", "sc_forward_ex", "sc_set_probe_limit",
+    "sc_build_neighbor_table_noalloc", "sc_build_map_async", "sc_map_status",
+    "LevelMap", "sc_subdivide", "sc_channel_to_spatial", "sc_build_level_map",
+    "sc_level_parents", "sc_get_level_map", "sc_conv_down", "sc_conv_up",
+    "sc_level_device_status", "sc_free_level_map",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -70,6 +74,10 @@ def load_library():
     P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     lib.sc_build_map.argtypes = [P, I64, I32, P]
     lib.sc_build_map.restype = P
+    lib.sc_build_map_async.argtypes = [P, I64, I32, I32, P]
+    lib.sc_build_map_async.restype = P
+    lib.sc_map_status.argtypes = [P]
+    lib.sc_map_status.restype = ctypes.c_int
     lib.sc_forward.argtypes = [P, P, P, P, P, I32, I32, ctypes.c_int, P]
     lib.sc_forward.restype = ctypes.c_int
     lib.sc_forward_ex.argtypes = [P, P, P, P, P, P, I32, I32, ctypes.c_int, ctypes.c_int,
@@ -94,6 +102,28 @@ def load_library():
     lib.sc_set_deterministic.restype = ctypes.c_int
     lib.sc_kernel_launches.restype = ctypes.c_uint64
     lib.sc_release_cached_memory.restype = ctypes.c_int
+    lib.sc_set_probe_limit.argtypes = [I32]
+    lib.sc_set_probe_limit.restype = ctypes.c_int
+    lib.sc_build_neighbor_table_noalloc.argtypes = [P, I64, I32, P, P, P]
+    lib.sc_build_neighbor_table_noalloc.restype = ctypes.c_int
+    lib.sc_subdivide.argtypes = [P, P, I64, I32, P, P, P, P, P, P]
+    lib.sc_subdivide.restype = ctypes.c_int
+    lib.sc_channel_to_spatial.argtypes = [P, P, P, I64, I32, ctypes.c_int, P, P]
+    lib.sc_channel_to_spatial.restype = ctypes.c_int
+    lib.sc_build_level_map.argtypes = [P, I64, I32, I32, P]
+    lib.sc_build_level_map.restype = P
+    lib.sc_level_parents.argtypes = [P]
+    lib.sc_level_parents.restype = I64
+    lib.sc_get_level_map.argtypes = [P, P, P, P, P]
+    lib.sc_get_level_map.restype = ctypes.c_int
+    for name in ("sc_conv_down", "sc_conv_up"):
+        getattr(lib, name).argtypes = [P, P, P, P, P, P, I32, I32, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, P]
+        getattr(lib, name).restype = ctypes.c_int
+    lib.sc_level_device_status.argtypes = [P, P]
+    lib.sc_level_device_status.restype = ctypes.c_int
+    lib.sc_free_level_map.argtypes = [P, P]
+    lib.sc_free_level_map.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -123,6 +153,12 @@ def sc_release_cached_memory() -> None:
 def sc_set_deterministic(enable: bool) -> None:
     """Bit-identical repeated forwards (see sc_set_deterministic in sc.h)."""
     _check(load_library().sc_set_deterministic(1 if enable else 0))
+
+
+def sc_set_probe_limit(limit: int) -> None:
+    """Cap on one key's insertion probes, for testing the bounded probe loop
+    (0 = the table's capacity; see sc_set_probe_limit in sc.h)."""
+    _check(load_library().sc_set_probe_limit(int(limit)))
 
 
 def _check(rc: int):
@@ -189,6 +225,43 @@ def sc_build_map(coords, res: int, stream=None) -> Map:
     if not ptr:
         raise ScError(sc_last_error(), sc_last_error_msg())
     return Map(ptr, int(coords.shape[0]), int(res), coords.device)
+
+
+def sc_build_neighbor_table_noalloc(coords, res: int, out=None, stream=None):
+    """int32 [N,27] neighbour table built without any device allocation by the
+    library (static scratch; N <= 2^19); returns (table, pair count)."""
+    import torch
+    if coords.dtype != torch.int32 or coords.dim() != 2 or coords.shape[1] != 4:
+        raise ValueError("coords must be int32 [N,4]")
+    n = coords.shape[0]
+    if out is None:
+        out = torch.empty((n, 27), dtype=torch.int32, device=coords.device)
+    elif out.dtype != torch.int32 or tuple(out.shape) != (n, 27):
+        raise ValueError("out must be int32 [N, 27]")
+    pairs = ctypes.c_int64(0)
+    _check(load_library().sc_build_neighbor_table_noalloc(
+        _dev_ptr(coords, "coords"), n, int(res), _dev_ptr(out, "out"), ctypes.byref(pairs),
+        _stream_ptr(stream)))
+    return out, int(pairs.value)
+
+
+def sc_build_map_async(coords, res: int, nbatch: int, stream=None) -> Map:
+    """sc_build_map without a host synchronisation; batch indices must lie in
+    [0, nbatch).  Device-found errors surface at sc_map_status / pairs."""
+    import torch
+    if coords.dtype != torch.int32 or coords.dim() != 2 or coords.shape[1] != 4:
+        raise ValueError("coords must be int32 [N,4]")
+    lib = load_library()
+    ptr = lib.sc_build_map_async(_dev_ptr(coords, "coords"), coords.shape[0], int(res),
+                                 int(nbatch), _stream_ptr(stream))
+    if not ptr:
+        raise ScError(sc_last_error(), sc_last_error_msg())
+    return Map(ptr, int(coords.shape[0]), int(res), coords.device)
+
+
+def sc_map_status(m: Map) -> None:
+    """Wait for the map's build and raise its error, if any."""
+    _check(load_library().sc_map_status(ctypes.c_void_p(m.ptr)))
 
 
 def sc_free_map(m: Map, stream=None):
@@ -315,3 +388,170 @@ def sc_get_pairs(m: Map, stream=None):
 def sc_device_status(m: Map, stream=None):
     """Synchronise and raise if a kernel over this map recorded a device error."""
     _check(load_library().sc_device_status(ctypes.c_void_p(m.ptr), _stream_ptr(stream)))
+
+
+# ---------------------------------------------------------------------------
+# level changes
+
+
+class LevelMap:
+    """A level map built by sc_build_level_map (owns its device memory)."""
+
+    def __init__(self, ptr: int, n: int, np_: int, device):
+        self.ptr = ptr
+        self.n = n
+        self.parents = np_
+        self.device = device
+
+    def free(self, stream=None):
+        if self.ptr:
+            sc_free_level_map(self, stream)
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.free()
+
+    def __del__(self):
+        try:
+            if self.ptr:
+                self.free()
+        except Exception:
+            pass
+
+
+def _coords_arg(coords):
+    import torch
+    if coords.dtype != torch.int32 or coords.dim() != 2 or coords.shape[1] != 4:
+        raise ValueError("coords must be int32 [N,4]")
+    return _dev_ptr(coords, "coords")
+
+
+def sc_subdivide(coords, res: int, mask=None, stream=None):
+    """Children of each voxel under an 8-bit mask (None: all 8).  Returns
+    (child_coords int32 [M,4], parent int32 [M], offset int32 [M], child_of
+    int32 [N,8]) on the device."""
+    import torch
+    cp = _coords_arg(coords)
+    n = coords.shape[0]
+    if mask is not None and (mask.dtype != torch.uint8 or mask.numel() != n):
+        raise ValueError("mask must be uint8 [N]")
+    dev = coords.device
+    cap = max(8 * n, 1)
+    child = torch.empty((cap, 4), dtype=torch.int32, device=dev)
+    parent = torch.empty(cap, dtype=torch.int32, device=dev)
+    offset = torch.empty(cap, dtype=torch.int32, device=dev)
+    child_of = torch.empty((max(n, 1), 8), dtype=torch.int32, device=dev)
+    m = ctypes.c_int64(0)
+    _check(load_library().sc_subdivide(cp, _dev_ptr(mask, "mask"), n, int(res),
+                                       _dev_ptr(child, "child_coords"), _dev_ptr(parent, "parent"),
+                                       _dev_ptr(offset, "offset"), _dev_ptr(child_of, "child_of"),
+                                       ctypes.byref(m), _stream_ptr(stream)))
+    M = int(m.value)
+    return child[:M], parent[:M], offset[:M], child_of[:n]
+
+
+def sc_channel_to_spatial(feats, parent, offset, stream=None):
+    """Channel2Spatial: child (parent i, offset o) takes channels c*8 + o of
+    feats[i] (feats [N, 8C]); returns [M, C] in feats' dtype."""
+    import torch
+    n, c8 = feats.shape
+    if c8 % 8:
+        raise ValueError("feats must have 8C channels")
+    m = parent.numel()
+    out = torch.empty((m, c8 // 8), dtype=feats.dtype, device=feats.device)
+    _check(load_library().sc_channel_to_spatial(
+        _dev_ptr(feats, "feats"), _dev_ptr(parent, "parent"), _dev_ptr(offset, "offset"), m,
+        c8 // 8, _operand_dtype(feats), _dev_ptr(out, "out"), _stream_ptr(stream)))
+    return out
+
+
+def sc_build_level_map(coords, res: int, nbatch: int = 1, stream=None) -> LevelMap:
+    """Parents (b, x>>1, y>>1, z>>1) of fine voxels, in (b,x,y,z) order, with
+    their child tables; drives sc_conv_down / sc_conv_up."""
+    lib = load_library()
+    ptr = lib.sc_build_level_map(_coords_arg(coords), coords.shape[0], int(res), int(nbatch),
+                                 _stream_ptr(stream))
+    if not ptr:
+        raise ScError(sc_last_error(), sc_last_error_msg())
+    np_ = int(lib.sc_level_parents(ctypes.c_void_p(ptr)))
+    return LevelMap(ptr, int(coords.shape[0]), np_, coords.device)
+
+
+def sc_level_parents(lm: LevelMap) -> int:
+    v = load_library().sc_level_parents(ctypes.c_void_p(lm.ptr))
+    if v < 0:
+        raise ScError(sc_last_error(), sc_last_error_msg())
+    return int(v)
+
+
+def sc_get_level_map(lm: LevelMap, stream=None):
+    """(parent_coords int32 [P,4], child_of int32 [P,8], parent_of int32 [N])."""
+    import torch
+    P = lm.parents
+    pc = torch.empty((max(P, 1), 4), dtype=torch.int32, device=lm.device)
+    co = torch.empty((max(P, 1), 8), dtype=torch.int32, device=lm.device)
+    po = torch.empty(max(lm.n, 1), dtype=torch.int32, device=lm.device)
+    _check(load_library().sc_get_level_map(ctypes.c_void_p(lm.ptr), _dev_ptr(pc, "pc"),
+                                           _dev_ptr(co, "co"), _dev_ptr(po, "po"),
+                                           _stream_ptr(stream)))
+    return pc[:P], co[:P], po[:lm.n]
+
+
+def _level_conv(fn, lm, feats, weight, bias, residual, act, out_dtype, out, n_out, stream):
+    import torch
+    if feats.dtype != weight.dtype:
+        raise ValueError("feats and weight must have the same dtype")
+    dt = _operand_dtype(feats)
+    if act not in _ACTS:
+        raise ValueError("act must be one of %s" % sorted(_ACTS))
+    out_dtype = torch.float32 if out_dtype is None else out_dtype
+    odts = {torch.float32: SC_F32, torch.bfloat16: SC_BF16, torch.float16: SC_F16}
+    if out_dtype not in odts:
+        raise ValueError("out_dtype must be float32, bfloat16 or float16")
+    cin = feats.shape[1]
+    if weight.dim() != 3 or weight.shape[0] != 8 or weight.shape[1] != cin:
+        raise ValueError("weight must be [8, cin, cout]")
+    cout = weight.shape[2]
+    if bias is not None and (bias.dtype != torch.float32 or bias.numel() != cout):
+        raise ValueError("bias must be fp32 [cout]")
+    if residual is not None and (residual.dtype != out_dtype or
+                                 tuple(residual.shape) != (n_out, cout)):
+        raise ValueError("residual must be [rows, cout] in out_dtype")
+    if out is None:
+        out = torch.empty((n_out, cout), dtype=out_dtype, device=feats.device)
+    rc = fn(ctypes.c_void_p(lm.ptr), _dev_ptr(feats, "feats"), _dev_ptr(weight, "weight"),
+            _dev_ptr(bias, "bias"), _dev_ptr(residual, "residual"), _dev_ptr(out, "out"), cin,
+            cout, dt, _ACTS[act], odts[out_dtype], _stream_ptr(stream))
+    _check(rc)
+    return out
+
+
+def sc_conv_down(lm: LevelMap, feats, weight, bias=None, residual=None, act="none",
+                 out_dtype=None, out=None, stream=None):
+    """2x2x2 stride-2 convolution to the parents: feats [N, cin] -> [P, cout]."""
+    if feats.shape[0] != lm.n:
+        raise ValueError("feats has %d rows, the level map %d fine rows" % (feats.shape[0], lm.n))
+    return _level_conv(load_library().sc_conv_down, lm, feats, weight, bias, residual, act,
+                       out_dtype, out, lm.parents, stream)
+
+
+def sc_conv_up(lm: LevelMap, feats, weight, bias=None, residual=None, act="none",
+               out_dtype=None, out=None, stream=None):
+    """Its transpose: parent feats [P, cin] -> fine [N, cout]."""
+    if feats.shape[0] != lm.parents:
+        raise ValueError("feats has %d rows, the level map %d parents" % (feats.shape[0],
+                                                                          lm.parents))
+    return _level_conv(load_library().sc_conv_up, lm, feats, weight, bias, residual, act,
+                       out_dtype, out, lm.n, stream)
+
+
+def sc_level_device_status(lm: LevelMap, stream=None):
+    _check(load_library().sc_level_device_status(ctypes.c_void_p(lm.ptr), _stream_ptr(stream)))
+
+
+def sc_free_level_map(lm: LevelMap, stream=None):
+    rc = load_library().sc_free_level_map(ctypes.c_void_p(lm.ptr), _stream_ptr(stream))
+    lm.ptr = 0
+    _check(rc)

@@ -36,19 +36,22 @@ __device__ __forceinline__ void cp_async_16_ca(void* dst, const void* src) {
 
 template <int J>  // columns per lane = J, cout <= 32 * J
 __global__ void __launch_bounds__(kSimtWarps * 32) k_conv_simt_f32(
-    const int32_t* __restrict__ nbr, int64_t n, const float* __restrict__ feats,
-    const float* __restrict__ w, const Epilogue ep, int cin, int cout) {
+    const int32_t* __restrict__ nbr, const int32_t* __restrict__ row_of, int64_t n, int taps,
+    const float* __restrict__ feats, const float* __restrict__ w, const Epilogue ep, int cin,
+    int cout) {
   __shared__ float s_a[kSimtWarps][kTaps][32];
   __shared__ uint32_t s_mask[kSimtWarps];
   extern __shared__ __align__(16) float s_w[];  // [2][32][32 * J]
   constexpr int kWStride = 32 * J;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t o = (int64_t)blockIdx.x * kSimtWarps + warp;
-  const bool valid = o < n;
-  // tile-major table: row o of tile o / 128, offset k at [tile][k][o % 128]
+  const int64_t o = (int64_t)blockIdx.x * kSimtWarps + warp;  // tile position
+  // output row of the position (-1: none)
+  const int32_t orow = o < n ? (row_of ? __ldg(row_of + o) : (int32_t)o) : -1;
+  const bool valid = orow >= 0;
+  // tile-major table: position o of tile o / 128, offset k at [tile][k][o % 128]
   const int32_t nb =
-      (valid && lane < kTaps)
-          ? __ldg(nbr + (o / kTileRows) * (kTileRows * kTaps) + lane * kTileRows + (o % kTileRows))
+      (valid && lane < taps)
+          ? __ldg(nbr + (o / kTileRows) * (kTileRows * taps) + lane * kTileRows + (o % kTileRows))
           : -1;
   const uint32_t present = __ballot_sync(0xffffffffu, nb >= 0);
   if (lane == 0) s_mask[warp] = present;
@@ -87,6 +90,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) k_conv_simt_f32(
     if (rem) stage_w(__ffs(rem) - 1, ci0, width, 0);
 #pragma unroll
     for (int k = 0; k < kTaps; ++k) {
+      if (k >= taps) break;
       const int32_t i = __shfl_sync(0xffffffffu, nb, k);
       s_a[warp][k][lane] =
           (i >= 0 && lane < width) ? __ldg(feats + (int64_t)i * cin + ci0 + lane) : 0.f;
@@ -120,7 +124,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) k_conv_simt_f32(
     for (int j = 0; j < J; ++j) {
       const int c = lane + 32 * j;
       if (c >= cout) continue;
-      const int64_t e = o * cout + c;
+      const int64_t e = (int64_t)orow * cout + c;
       float v = apply_act(acc[j] + (ep.bias ? __ldg(ep.bias + c) : 0.f), ep.act);
       if (ep.out_half == kOutBf16) {
         if (ep.residual)
@@ -138,7 +142,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) k_conv_simt_f32(
 }
 
 template <int J>
-cudaError_t launch_simt(const sc_map* m, const float* feats, const float* w, const Epilogue& ep,
+cudaError_t launch_simt(const ConvMap& m, const float* feats, const float* w, const Epilogue& ep,
                         int cin, int cout, cudaStream_t s) {
   const size_t smem = 2ull * 32 * 32 * J * sizeof(float);
   // Opt-in above 48 KB of dynamic shared memory, once per device (function
@@ -155,13 +159,14 @@ cudaError_t launch_simt(const sc_map* m, const float* feats, const float* w, con
     if (e != cudaSuccess) return e;
     attr_set[dev].store(true, std::memory_order_release);
   }
-  const unsigned blocks = (unsigned)((m->n + kSimtWarps - 1) / kSimtWarps);
-  k_conv_simt_f32<J><<<blocks, kSimtWarps * 32, smem, s>>>(m->nbr, m->n, feats, w, ep, cin, cout);
+  const unsigned blocks = (unsigned)((m.n + kSimtWarps - 1) / kSimtWarps);
+  k_conv_simt_f32<J><<<blocks, kSimtWarps * 32, smem, s>>>(m.nbr, m.row_of, m.n, m.taps, feats, w,
+                                                           ep, cin, cout);
   note_launches(1);
   return cudaGetLastError();
 }
 
-cudaError_t launch_conv_simt_f32(const sc_map* m, const float* feats, const float* w,
+cudaError_t launch_conv_simt_f32(const ConvMap& m, const float* feats, const float* w,
                                  const Epilogue& ep, int cin, int cout, cudaStream_t s) {
   const int J = (cout + 31) / 32;
   if (J <= 1) return launch_simt<1>(m, feats, w, ep, cin, cout, s);

@@ -94,7 +94,7 @@ constexpr int kMmaWarp = 5 + kProducerWarps;
 constexpr int kTcThreads = 32 * (kMmaWarp + 1);
 
 constexpr int kSmemLimit = 227 * 1024;                  // opt-in dynamic shared memory per CTA
-constexpr int kNbrBytes = kTileRows * kTaps * 4;        // one tile's neighbour block, 13,824 B
+constexpr int kNbrBytes = kTileRows * kTaps * 4;        // a tile's neighbour block, <= 13,824 B
 // Epilogue staging: each epilogue warp transposes its 32 rows x 32 columns
 // through shared memory (row stride 36 floats: 16-byte aligned, and both the
 // row-wise writes and the column-group reads are bank-conflict-free).
@@ -138,8 +138,11 @@ struct TcCfg {
 
 struct TcArgs {
   const __nv_bfloat16* feats;  // [n][cin]
-  const int32_t* nbr;          // tile-major [ntiles][27][128], pad rows -1
+  const int32_t* nbr;          // tile-major [ntiles][taps][128], pad rows -1
   const uint32_t* tile_mask;   // [ntiles]
+  const int32_t* row_of;       // output row of each tile position (-1: none), or nullptr: the
+                               // position itself
+  int taps;                    // 27 (3x3x3) or 8 (2x2x2 between levels)
   const float* bias;
   const void* residual;  // [n][cout] in the output dtype, or nullptr
   void* out;             // fp32 or bf16 [n][cout]
@@ -147,7 +150,7 @@ struct TcArgs {
   int out_half;          // 16-bit output (kOutBf16 / kOutF16, nearest even), 0: fp32
   uint32_t idesc;        // MMA instruction descriptor (bf16 or fp16 operands)
   uint32_t* status;
-  int64_t n;
+  int64_t n;       // tile positions that hold an output row
   int64_t ntiles;
   int64_t whole;   // units 0 .. whole-1 are one work item each
   int64_t tail;    // units whole .. whole+tail-1 are `split` items each
@@ -219,13 +222,15 @@ __device__ __forceinline__ int unit_stages(uint32_t mask, int cin) {
 
 // Walks the K slices of a unit in order: for CS == 64, each present offset
 // k (ascending) with its cin/64 channel blocks; for CS < 64, the present
-// offsets 64/CS at a time (kTaps pads the last stage).  next() fills the
-// stage's offsets and returns its first channel.
+// offsets 64/CS at a time (k = taps, one past the last offset, pads the last
+// stage: its W box lies past the end of W and is zero-filled).  next() fills
+// the stage's offsets and returns its first channel.
 template <int CS>
 struct OffsetIter {
   uint32_t rem;
-  int cblk = 0, cblocks;
-  __device__ __forceinline__ OffsetIter(uint32_t mask, int cin) : rem(mask), cblocks(cin >> 6) {}
+  int cblk = 0, cblocks, taps;
+  __device__ __forceinline__ OffsetIter(uint32_t mask, int cin, int taps_)
+      : rem(mask), cblocks(cin >> 6), taps(taps_) {}
   // Step over the first `n` stages.
   __device__ __forceinline__ void skip(int n) {
     if constexpr (CS == 64) {
@@ -250,7 +255,7 @@ struct OffsetIter {
     } else {
 #pragma unroll
       for (int j = 0; j < 64 / CS; ++j) {
-        ks[j] = rem ? __ffs(rem) - 1 : kTaps;
+        ks[j] = rem ? __ffs(rem) - 1 : taps;
         rem &= rem - 1u;
       }
       return 0;
@@ -343,8 +348,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!mbar_wait_bounded(&nbr_empty[b], ((fills >> b) & 1u) ^ 1u, abort_flag))
             return false;
         }
-        mbar_arrive_expect_tx(&nbr_full[b], kNbrBytes);
-        bulk_copy_g2s(s_nbr + b * kTileRows * kTaps, p.nbr + t * (kTileRows * kTaps), kNbrBytes,
+        const uint32_t nbytes = (uint32_t)(p.taps * kTileRows * 4);
+        mbar_arrive_expect_tx(&nbr_full[b], nbytes);
+        bulk_copy_g2s(s_nbr + b * kTileRows * kTaps, p.nbr + t * (kTileRows * p.taps), nbytes,
                       &nbr_full[b]);
         fills ^= 1u << b;        // parity of the fills of buffer b
         fills |= 1u << (2 + b);  // buffer b used at least once
@@ -362,7 +368,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
         }
-        OffsetIter<CS> it(mask, p.cin);
+        OffsetIter<CS> it(mask, p.cin, p.taps);
         it.skip(s0);
         for (int s = s0; s < s1; ++s) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
@@ -445,7 +451,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         nbr_phase ^= 1u << buf;
       }
       const int32_t* nb = s_nbr + buf * (kTileRows * kTaps);
-      OffsetIter<CS> it(mask, p.cin);
+      OffsetIter<CS> it(mask, p.cin, p.taps);
       it.skip(s0);
       for (int s = s0; s < s1; ++s) {
         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
@@ -471,7 +477,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int jj = 1; jj < C::kSegs; ++jj)
             if (j == jj) k = ks[jj];
-          src_rows[i] = (has_rows && k < kTaps) ? nb[k * kTileRows + r] : -1;
+          src_rows[i] = (has_rows && k < p.taps) ? nb[k * kTileRows + r] : -1;
         }
 #pragma unroll
         for (int i = 0; i < C::kPerThread; ++i) {
@@ -581,11 +587,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float bscale = last ? 1.f : 0.f;
       const bool resid = FUSED && p.residual != nullptr && last;
       const int64_t wrow0 = (wi.unit * CL + rank) * kTileRows + warp * 32;  // this warp's rows
-      if (resid && wrow0 + lane < p.n) {
+      // Output row of this lane's position (-1: a pad position); the stores
+      // below take the rows of other lanes by shuffle.
+      const int64_t my_pos = wrow0 + lane;
+      const int32_t my_row =
+          my_pos < p.n ? (p.row_of ? __ldg(p.row_of + my_pos) : (int32_t)my_pos) : -1;
+      if (resid && my_row >= 0) {
         // This thread's row of the residual into L2 while the main loop runs
         // (128-byte lines); the column-group loads below then hit L2.
         const int rbytes = p.cout * (p.out_half ? 2 : 4);
-        const char* rrow = static_cast<const char*>(p.residual) + (wrow0 + lane) * rbytes;
+        const char* rrow = static_cast<const char*>(p.residual) + (int64_t)my_row * rbytes;
         for (int off = 0; off < rbytes; off += 128)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(rrow + off));
       }
@@ -607,10 +618,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int qq = 0; qq < 4; ++qq) {
           const int q = 4 * h + qq;
           const int c = ch * 32 + 4 * (lane & 7);
-          const int64_t row = wrow0 + 4 * q + (lane >> 3);
+          const int32_t row = __shfl_sync(0xffffffffu, my_row, 4 * q + (lane >> 3));
           rv[qq] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (resid && row < p.n && c < p.cout) {
-            const int64_t e = row * p.cout + c;
+          if (resid && row >= 0 && c < p.cout) {
+            const int64_t e = (int64_t)row * p.cout + c;
             if (p.out_half) {
               const uint2 rb = __ldg(reinterpret_cast<const uint2*>(
                   static_cast<const __nv_bfloat16*>(p.residual) + e));
@@ -640,10 +651,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int q = 4 * h + qq;
           const int r = 4 * q + (lane >> 3), g = lane & 7;
           const int c = ch * 32 + 4 * g;
-          const int64_t row = wrow0 + r;
+          const int32_t row = __shfl_sync(0xffffffffu, my_row, r);
           float4 o = *reinterpret_cast<const float4*>(stg + r * kStageRow + 4 * g);
-          if (row < p.n && c < p.cout) {
-            const int64_t e = row * p.cout + c;
+          if (row >= 0 && c < p.cout) {
+            const int64_t e = (int64_t)row * p.cout + c;
             if (p.act) {
               o.x = apply_act(o.x, p.act);
               o.y = apply_act(o.y, p.act);
@@ -681,8 +692,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int ch = 0; ch < nchunks; ++ch) {
         // Residual loads are issued early (the first half before the TMEM
         // load, the second before the first half is stored), so their L2
-        // latency overlaps work; out and residual may alias, so no load can
-        // move past a store by itself.
+        // latency overlaps work; out and residual may be one buffer (in
+        // place: each element is read, then written, by this thread), so no
+        // load can move past a store by itself.
         float4 ra[4], rb[4];
         if constexpr (FUSED) load_resid(ch, 0, ra);
         uint32_t v[32];
@@ -710,11 +722,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int q = 0; q < 8; ++q) {
             const int r = 4 * q + (lane >> 3), g = lane & 7;
             const int c = ch * 32 + 4 * g;
-            const int64_t row = wrow0 + r;
+            const int32_t row = __shfl_sync(0xffffffffu, my_row, r);
             const float4 o = *reinterpret_cast<const float4*>(stg + r * kStageRow + 4 * g);
-            if (row < p.n && c < p.cout) {
+            if (row >= 0 && c < p.cout) {
               float4* dst =
-                  reinterpret_cast<float4*>(static_cast<float*>(p.out) + row * p.cout + c);
+                  reinterpret_cast<float4*>(static_cast<float*>(p.out) + (int64_t)row * p.cout + c);
               if (add)
                 atomicAdd(dst, o);
               else
@@ -836,7 +848,7 @@ int tail_split(int64_t nunits, int64_t G, int max_stages) {
 }
 
 template <int NPAD, int CS, int CL, bool FUSED>
-cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, bool f16,
+cudaError_t launch_typed(const ConvMap& m, const void* feats, const void* w, bool f16,
                          const Epilogue& ep, int cin, int cout, cudaStream_t s) {
   using C = TcCfg<NPAD, CS>;
   auto kern = k_conv_tc<NPAD, CS, CL, FUSED>;
@@ -881,30 +893,37 @@ cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, bool
   }
 
   alignas(64) CUtensorMap tm_b;
-  if (!encode_2d(&tm_b, w, (uint64_t)cout, (uint64_t)kTaps * cin, (uint64_t)cout * 2, 64, CS,
+  if (!encode_2d(&tm_b, w, (uint64_t)cout, (uint64_t)m.taps * cin, (uint64_t)cout * 2, 64, CS,
                  CU_TENSOR_MAP_SWIZZLE_128B,
                  f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
     return cudaErrorInvalidValue;
   TcArgs a;
   a.feats = static_cast<const __nv_bfloat16*>(feats);
-  a.nbr = m->nbr;
-  a.tile_mask = m->tile_mask;
+  a.nbr = m.nbr;
+  a.tile_mask = m.tile_mask;
+  a.row_of = m.row_of;
+  a.taps = m.taps;
   a.bias = ep.bias;
   a.residual = ep.residual;
   a.out = ep.out;
   a.act = ep.act;
   a.out_half = ep.out_half;
   a.idesc = idesc_bf16_f32(kTileRows, NPAD, f16);
-  a.status = m->d_status;
-  a.n = m->n;
-  a.ntiles = m->ntiles;
+  a.status = m.status;
+  a.n = m.n;
+  a.ntiles = m.ntiles;
   a.cin = cin;
   a.cout = cout;
-  const int64_t nunits = (m->ntiles + CL - 1) / CL;
+  const int64_t nunits = (m.ntiles + CL - 1) / CL;
   if (nunits == 0) return cudaSuccess;
-  const int max_stages = CS == 64 ? kTaps * (cin / 64) : (kTaps + 64 / CS - 1) / (64 / CS);
-  // An activation or a bf16 output cannot be applied to partial sums.
-  const int split = (ep.act || ep.out_half) ? 1 : tail_split(nunits, max_clusters, max_stages);
+  const int max_stages = CS == 64 ? m.taps * (cin / 64) : (m.taps + 64 / CS - 1) / (64 / CS);
+  // An activation or a 16-bit output cannot be applied to partial sums.  In
+  // place (residual == out), the split rows would be zeroed, and other parts'
+  // sums added, before the last part reads the residual from them.
+  // With a row indirection the split rows are not one range to zero.
+  const bool unsplit =
+      ep.act || ep.out_half || (ep.residual && ep.residual == ep.out) || m.row_of != nullptr;
+  const int split = unsplit ? 1 : tail_split(nunits, max_clusters, max_stages);
   a.split = split;
   a.tail = split > 1 ? (nunits >= max_clusters ? nunits % max_clusters : nunits) : 0;
   a.whole = nunits - a.tail;
@@ -914,7 +933,7 @@ cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, bool
     // The split units' rows start at zero; their parts add into them.  The
     // convolution is this launch's programmatic dependent (attribute 1).
     const int64_t row0 = a.whole * CL * kTileRows;
-    const int64_t n4 = (m->n - row0) * cout / 4;  // cout is a multiple of 16
+    const int64_t n4 = (m.n - row0) * cout / 4;  // cout is a multiple of 16
     const int64_t zb = std::min<int64_t>((n4 + 255) / 256, 2 * 148);
     k_zero_rows<<<(unsigned)zb, 256, 0, s>>>(
         reinterpret_cast<float4*>(static_cast<float*>(ep.out) + row0 * cout), n4);
@@ -931,7 +950,7 @@ cudaError_t launch_typed(const sc_map* m, const void* feats, const void* w, bool
 }
 
 template <int NPAD, int CS>
-cudaError_t launch_cl(const sc_map* m, const void* feats, const void* w, bool f16,
+cudaError_t launch_cl(const ConvMap& m, const void* feats, const void* w, bool f16,
                       const Epilogue& ep, int cin, int cout, cudaStream_t s) {
   const bool fused = ep.act || ep.residual || ep.out_half;
   if (cluster_size(NPAD) == 2)
@@ -942,7 +961,7 @@ cudaError_t launch_cl(const sc_map* m, const void* feats, const void* w, bool f1
 }
 
 template <int NPAD>
-cudaError_t launch_npad(const sc_map* m, const void* feats, const void* w, bool f16,
+cudaError_t launch_npad(const ConvMap& m, const void* feats, const void* w, bool f16,
                         const Epilogue& ep, int cin, int cout, cudaStream_t s) {
   if (cin == 16) return launch_cl<NPAD, 16>(m, feats, w, f16, ep, cin, cout, s);
   if (cin == 32) return launch_cl<NPAD, 32>(m, feats, w, f16, ep, cin, cout, s);
@@ -959,7 +978,7 @@ bool conv_tc_supported(int cin, int cout) {
   return cin_ok && cout_ok;
 }
 
-cudaError_t launch_conv_tc(const sc_map* m, const void* feats, const void* w, bool f16,
+cudaError_t launch_conv_tc(const ConvMap& m, const void* feats, const void* w, bool f16,
                            const Epilogue& ep, int cin, int cout, cudaStream_t s) {
   if (!conv_tc_supported(cin, cout)) return cudaErrorNotSupported;
   const int npad = (cout + 63) / 64 * 64;

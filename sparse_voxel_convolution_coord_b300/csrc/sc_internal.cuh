@@ -66,7 +66,12 @@ struct HashParams {
   int bres;            // bricks per axis: (res + 1) / 2
   uint64_t bmax;       // batch indices must be < bmax
   int64_t n;
+  uint64_t probe_limit;  // slots an insertion may probe before reporting a full table
 };
+
+// Process-wide cap on an insertion's probes (sc_set_probe_limit); 0 = none
+// beyond the table's capacity.
+uint32_t probe_limit_setting();
 
 __device__ __forceinline__ uint64_t cell_key(const HashParams& hp, int b, int x, int y, int z) {
   const uint64_t r = (uint64_t)hp.res;
@@ -121,6 +126,8 @@ inline bool make_hash_params(HashParams& hp, uint64_t* slots, int64_t n, int res
   hp.res = res;
   hp.bres = (res + 1) / 2;
   hp.n = n;
+  const uint64_t lim = probe_limit_setting();
+  hp.probe_limit = (lim && lim < (1ull << log2cap)) ? lim : (1ull << log2cap);
   hp.k32 = k32_allowed && log2cap <= 32 && res3 <= 0xffffffffull;
   if (hp.k32) {
     hp.bmax = 0xffffffffull / res3;  // keys <= 2^32 - 2: a live slot is never all ones
@@ -403,6 +410,13 @@ struct sc_map {
   void* (*alloc)(size_t, void*, void*);
   void (*free_fn)(void*, void*, void*);
   void* alloc_ctx;
+  // Builds that did not synchronise (sc_build_map_async): until `pending` is
+  // cleared by the first call that needs the result, the status words and
+  // the pair count are only on the device; `built` is recorded after the
+  // build's kernels.  build_word keeps the build's status bits once read.
+  int pending;
+  cudaEvent_t built;
+  uint32_t build_word;
 };
 
 namespace sc {
@@ -443,13 +457,51 @@ __device__ __forceinline__ float apply_act(float v, int act) {
   return v;
 }
 
-cudaError_t launch_conv_simt_f32(const sc_map* m, const float* feats, const float* w,
+// What the convolution kernels read of a map: per 128-position tile, a
+// tile-major block of `taps` input rows per position (-1: absent), the
+// tile's offset mask, and optionally the output row of each position.
+struct ConvMap {
+  const int32_t* nbr;         // [ntiles][taps][128]
+  const uint32_t* tile_mask;  // [ntiles]
+  const int32_t* row_of;      // [ntiles * 128] output row (-1: none), or nullptr: identity
+  int64_t n;                  // positions 0 .. n-1 hold an output row
+  int64_t ntiles;
+  int taps;                   // 27 (3x3x3) or 8 (2x2x2 between levels)
+  uint32_t* status;           // device status word for bounded waits
+};
+inline ConvMap conv_map_of(const sc_map* m) {
+  return ConvMap{m->nbr, m->tile_mask, nullptr, m->n, m->ntiles, kTaps, m->d_status};
+}
+
+cudaError_t launch_conv_simt_f32(const ConvMap& m, const float* feats, const float* w,
                                  const Epilogue& ep, int cin, int cout, cudaStream_t s);
 // bf16 or fp16 operands (f16 = true); returns cudaErrorNotSupported for
 // shapes outside the tensor-core envelope.
-cudaError_t launch_conv_tc(const sc_map* m, const void* feats, const void* w, bool f16,
+cudaError_t launch_conv_tc(const ConvMap& m, const void* feats, const void* w, bool f16,
                            const Epilogue& ep, int cin, int cout, cudaStream_t s);
 bool conv_tc_supported(int cin, int cout);
+// Level changes (sc_levels.cu).
+cudaError_t launch_child_counts(const int32_t* coords, const uint8_t* mask, int64_t n, int res,
+                                int32_t* counts, uint32_t* status, cudaStream_t s);
+cudaError_t launch_subdivide(const int32_t* coords, const uint8_t* mask, int64_t n,
+                             const int32_t* first, int32_t* child_coords, int32_t* parent,
+                             int32_t* offset, int32_t* child_of, cudaStream_t s);
+cudaError_t launch_channel_to_spatial(const void* feats, const int32_t* parent,
+                                      const int32_t* offset, int64_t m, int c, int esize,
+                                      void* out, cudaStream_t s);
+size_t level_scratch_bytes(int64_t n, int kbytes);
+template <typename K>
+cudaError_t build_level_tables(const int32_t* coords, int64_t n, int res, int nbatch, int key_bits,
+                               void* scratch, int32_t* down_nbr, uint32_t* down_mask,
+                               int32_t* parent_of, int32_t* parent_coords, int32_t* up_nbr,
+                               int32_t* up_row, uint32_t* up_mask, int64_t* np_dev,
+                               uint32_t* status, cudaStream_t s);
+cudaError_t launch_child_table(const int32_t* down_nbr, int64_t np, int32_t* out, cudaStream_t s);
+// sc_sort.cu
+cudaError_t scan_exclusive(const int32_t* in, int32_t* out, int64_t len, int64_t* total,
+                           void* scratch, cudaStream_t s);
+size_t scan_scratch_bytes(int64_t len);
+
 // Process-wide count of the kernels this library has launched (host side).
 void note_launches(int k);
 uint32_t* status_readback_buffer();  // pinned, kStatusBlockBytes, per host thread

@@ -17,24 +17,28 @@
 //                    returns the occupant, so a duplicate key is seen when
 //                    its twin's slot is reached.  Errors are OR-reduced per
 //                    warp.
-//  k_neighbor_query  one thread per (voxel, neighbour column dx, dy): the
-//                    three neighbours dz = -1, 0, 1 of the column are probed
-//                    with three independent loads (brick-local homes put a
-//                    warp's loads, 32 consecutive voxels on one column, on
-//                    few cache lines), collisions followed along the probe
-//                    sequence.  Nine threads per voxel keep enough warps in
-//                    flight to hide the probe latency, which one thread per
-//                    voxel with 26 dependent resolutions could not.  The
+//  k_neighbor_query32  (32-bit keys) one thread per voxel: the 27 cells
+//                    around it fall in 2 x 2 x 2 bricks whose group hashes
+//                    follow from one by additions, so all 26 home-slot loads
+//                    are computed at once and issued independently; a lookup
+//                    stops at its home slot on its key, an empty slot, or
+//                    another key whose moved flag is clear, and the few
+//                    others follow their probe sequences afterwards.  The
 //                    tile-major output [tile][27][128] is written coalesced
-//                    (a warp writes 32 consecutive rows of one offset).  With
-//                    32-bit keys a lookup stops at its home slot unless that
-//                    slot's moved flag says a key homed there moved on.  Each
-//                    block ORs its rows' presence bits into the tile mask the
-//                    convolution uses to skip absent offsets, and adds its
-//                    pair count to one of 32 global counters.
+//                    (a warp writes 32 consecutive rows of one offset); a
+//                    block is one tile, so it stores the tile's offset mask
+//                    (which the convolution uses to skip absent offsets)
+//                    and adds its pair count to one of 32 global counters.
+//  k_neighbor_query  (64-bit keys) one thread per (voxel, neighbour column
+//                    dx, dy), its three lookups (dz = -1, 0, 1) probing
+//                    until their key or an empty slot.
+//  The insert and the query are launched as programmatic dependents of the
+//  kernel before them: they start while it finishes, read their coordinates,
+//  and wait for it (griddepcontrol.wait) before touching the table.
 //  k_pairs_*         CSR pair lists per offset (ascending output row),
 //                    built on demand: count, scan, scatter.
 #include <algorithm>
+#include <cstring>
 
 #include "sc_internal.cuh"
 
@@ -87,10 +91,16 @@ __global__ void __launch_bounds__(kInsertThreads) k_hash_insert(const int4* __re
     }
     home = pos;
   }
-  // Synchronous probing rounds; at most `capacity` rounds (every slot).
+  // Everything above read only the coordinates; the table is cleared by the
+  // kernel launched before this one (a programmatic dependency when launched
+  // with that attribute: wait for its completion here).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Synchronous probing rounds; at most hp.probe_limit rounds (every slot,
+  // unless sc_set_probe_limit set a smaller cap).
   for (uint64_t round = 0; __any_sync(0xffffffffu, pending); ++round) {
     if (!pending) continue;
-    if (round > hp.cap_mask) {
+    if (round >= hp.probe_limit) {
       err |= kStatTableFull;
       pending = false;
       continue;
@@ -264,6 +274,145 @@ __global__ void __launch_bounds__(kTileRows) k_neighbor_query(
   }
 }
 
+// 32-bit keys: one thread per voxel resolves all 26 neighbours.  The 27
+// cells around a voxel lie in 2 x 2 x 2 bricks (along each axis the bricks
+// (v - 1) >> 1 and the next), and the brick hash is linear in the brick
+// index, so the eight group hashes cost an add each; every neighbour's home
+// slot is its cell within its brick's group.  All 26 home loads are
+// independent, so a thread keeps many in flight; a lookup the home slot
+// does not settle (the moved flag of another key) continues after the main
+// pass along its probe sequence.  Rows of a 128-row tile are one block, so
+// the tile's offset mask is a plain store.  Tile-major output is written
+// straight out (a warp's stores of one offset are 32 consecutive rows);
+// row-major output is staged in shared memory and written out contiguously.
+template <NbrLayout L>
+__global__ void __launch_bounds__(kTileRows, 8) k_neighbor_query32(
+    const int4* __restrict__ coords, HashParams hp, int32_t* __restrict__ nbr,
+    uint32_t* __restrict__ tile_mask, unsigned long long* pair_count) {
+  __shared__ uint32_t s_or[kTileRows / 32];
+  __shared__ uint32_t s_cnt[kTileRows / 32];
+  __shared__ __align__(16) int32_t s_rows[L == kNbrRowMajor ? kTileRows * kTaps : 4];
+  const unsigned long long* slots = reinterpret_cast<const unsigned long long*>(hp.slots);
+  const int64_t row0 = (int64_t)blockIdx.x * kTileRows;
+  const int64_t o = row0 + threadIdx.x;
+  const bool valid = o < hp.n;
+  // A pad row sits far outside the grid, so that every neighbour is absent.
+  const int4 c = valid ? __ldg(coords + o) : make_int4(0, -4, -4, -4);
+  const uint32_t R = (uint32_t)hp.res, BR = (uint32_t)hp.bres;
+  const int x = c.y, y = c.z, z = c.w;
+  const uint32_t key0 = cell_key32(hp, c.x, x, y, z);
+  const int bx = (x - 1) >> 1, by = (y - 1) >> 1, bz = (z - 1) >> 1;
+  // brick(bx + i, by + j, bz + l) = brick000 + i BR^2 + j BR + l (mod 2^32),
+  // and so is its hash times the multiplier.
+  const uint32_t brick000 = (((uint32_t)c.x * BR + (uint32_t)bx) * BR + (uint32_t)by) * BR +
+                            (uint32_t)bz;
+  constexpr uint32_t kPhi = 0x9E3779B9u;
+  const uint32_t h000 = brick000 * kPhi, hA = BR * BR * kPhi, hB = BR * kPhi;
+  const int gshift = 32 - (hp.log2cap - 3);
+  const uint32_t RR = R * R;
+  int32_t* out_t = nbr + row0 * kTaps + threadIdx.x;  // tile-major: [k * 128]
+  int32_t* out_s = s_rows + threadIdx.x * kTaps;      // row-major staging: [k]
+  auto put = [&](int k, int32_t r) {
+    if constexpr (L == kNbrTileMajor)
+      out_t[k * kTileRows] = r;
+    else
+      out_s[k] = r;
+  };
+  // The table is written by the insert kernel launched before this one.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  uint32_t bits = 0, pend = 0;
+#pragma unroll
+  for (int col = 0; col < 9; ++col) {
+    const int dx = col / 3 - 1, dy = col % 3 - 1;
+    const int xx = x + dx, yy = y + dy;
+    const bool colin = (unsigned)xx < R && (unsigned)yy < R;
+    const uint32_t hxy =
+        h000 + (uint32_t)((xx >> 1) - bx) * hA + (uint32_t)((yy >> 1) - by) * hB;
+    const uint32_t cellxy = (uint32_t)(((xx & 1) << 2) | ((yy & 1) << 1));
+    const uint32_t kxy = key0 + (uint32_t)dx * RR + (uint32_t)dy * R;
+#pragma unroll
+    for (int jz = 0; jz < 3; ++jz) {
+      const int k = 3 * col + jz;
+      if (k == kCentre) continue;
+      const int zz = z + jz - 1;
+      const bool in = colin && (unsigned)zz < R;
+      const uint32_t slot = (((hxy + (uint32_t)((zz >> 1) - bz) * kPhi) >> gshift) << 3) |
+                            cellxy | (uint32_t)(zz & 1);
+      const unsigned long long sl = in ? __ldg(slots + slot) : kEmptySlot;
+      int32_t r = -1;
+      if (sl != kEmptySlot) {
+        if ((uint32_t)(sl >> 32) == kxy + (uint32_t)(jz - 1))
+          r = (int32_t)((uint32_t)sl & kRowMask32);
+        else if (sl & kMovedFlag)
+          pend |= 1u << k;
+      }
+      bits |= (r >= 0 ? 1u : 0u) << k;
+      put(k, r);
+    }
+  }
+  // Lookups that left their home slot: follow the probe sequence.
+  const uint32_t cmask = (uint32_t)hp.cap_mask;
+  while (pend) {
+    const int k = __ffs(pend) - 1;
+    pend &= pend - 1u;
+    const int dx = k / 9 - 1, dy = (k / 3) % 3 - 1, dz = k % 3 - 1;
+    const int xx = x + dx, yy = y + dy, zz = z + dz;
+    const uint32_t key = key0 + (uint32_t)dx * RR + (uint32_t)dy * R + (uint32_t)dz;
+    uint32_t pos = (((h000 + (uint32_t)((xx >> 1) - bx) * hA + (uint32_t)((yy >> 1) - by) * hB +
+                      (uint32_t)((zz >> 1) - bz) * kPhi) >>
+                     gshift)
+                    << 3) |
+                   (uint32_t)(((xx & 1) << 2) | ((yy & 1) << 1) | (zz & 1));
+    const uint32_t step = probe_step32(hp, key);
+    for (uint32_t it = 0; it < cmask; ++it) {
+      pos = (pos + step) & cmask;
+      const unsigned long long sl = __ldg(slots + pos);
+      if (sl == kEmptySlot) break;
+      if ((uint32_t)(sl >> 32) == key) {
+        put(k, (int32_t)((uint32_t)sl & kRowMask32));
+        bits |= 1u << k;
+        break;
+      }
+    }
+  }
+  put(kCentre, valid ? (int32_t)o : -1);
+  if (valid) bits |= 1u << kCentre;
+  // The tile's offsets present in any row (this block is the whole tile) and
+  // its pair count into one of the counters.
+  const int lane = threadIdx.x & 31;
+  const uint32_t wor = __reduce_or_sync(0xffffffffu, bits);
+  const uint32_t wcnt = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(bits));
+  if (lane == 0) {
+    s_or[threadIdx.x >> 5] = wor;
+    s_cnt[threadIdx.x >> 5] = wcnt;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t m = 0, bc = 0;
+#pragma unroll
+    for (int w = 0; w < kTileRows / 32; ++w) {
+      m |= s_or[w];
+      bc += s_cnt[w];
+    }
+    tile_mask[blockIdx.x] = m;
+    if (bc) atomicAdd(pair_count + blockIdx.x % kPairCounters, (unsigned long long)bc);
+  }
+  if constexpr (L == kNbrRowMajor) {
+    // The block's rows [row0, row0 + rows) are one contiguous range of
+    // rows * 27 ints: copy it out with 16-byte stores where aligned.
+    const int total = (int)min((int64_t)kTileRows, hp.n - row0) * kTaps;
+    int32_t* dst = nbr + row0 * kTaps;
+    if ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+      const int nvec = total >> 2;
+      for (int i = threadIdx.x; i < nvec; i += kTileRows)
+        reinterpret_cast<int4*>(dst)[i] = reinterpret_cast<const int4*>(s_rows)[i];
+      for (int i = (nvec << 2) + threadIdx.x; i < total; i += kTileRows) dst[i] = s_rows[i];
+    } else {
+      for (int i = threadIdx.x; i < total; i += kTileRows) dst[i] = s_rows[i];
+    }
+  }
+}
+
 // nbr_out[n][27] from the tile-major table: one block per tile, staged in
 // shared memory so that both sides are coalesced.
 __global__ void __launch_bounds__(kTileRows) k_nbr_to_row_major(const int32_t* __restrict__ nbr_t,
@@ -292,6 +441,9 @@ __global__ void __launch_bounds__(kTileRows) k_nbr_to_row_major(const int32_t* _
 __global__ void __launch_bounds__(256) k_map_init(ulonglong2* __restrict__ slots, int64_t npairs2,
                                                   uint32_t* __restrict__ tile_mask, int64_t ntiles,
                                                   uint32_t* __restrict__ status) {
+  // The insert kernel launched after this one may start at once: it reads
+  // coordinates first and waits for this grid before touching the table.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const ulonglong2 ones = make_ulonglong2(kEmptySlot, kEmptySlot);
@@ -312,18 +464,36 @@ cudaError_t launch_map_init(const HashParams& hp, uint32_t* tile_mask, int64_t n
   return cudaGetLastError();
 }
 
+// A launch with the programmatic-dependency attribute: the kernel may start
+// while the one before it in the stream finishes, and waits for it
+// (griddepcontrol.wait) before it reads that kernel's output.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kern)(Params...), unsigned blocks, unsigned threads,
+                             cudaStream_t s, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(blocks, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Params>(args)...);
+}
+
 cudaError_t launch_hash_insert(const int32_t* coords, const HashParams& hp, uint32_t* status,
                                cudaStream_t s) {
   if (hp.n == 0) return cudaSuccess;
-  const int64_t blocks = (hp.n + kInsertThreads - 1) / kInsertThreads;
-  if (hp.k32)
-    k_hash_insert<true><<<(unsigned)blocks, kInsertThreads, 0, s>>>(
-        reinterpret_cast<const int4*>(coords), hp, status);
-  else
-    k_hash_insert<false><<<(unsigned)blocks, kInsertThreads, 0, s>>>(
-        reinterpret_cast<const int4*>(coords), hp, status);
-  note_launches(1);
-  return cudaGetLastError();
+  const unsigned blocks = (unsigned)((hp.n + kInsertThreads - 1) / kInsertThreads);
+  const int4* c4 = reinterpret_cast<const int4*>(coords);
+  cudaError_t e = hp.k32 ? launch_dependent(k_hash_insert<true>, blocks, kInsertThreads, s, c4,
+                                            hp, status)
+                         : launch_dependent(k_hash_insert<false>, blocks, kInsertThreads, s, c4,
+                                            hp, status);
+  if (e == cudaSuccess) note_launches(1);
+  return e;
 }
 
 cudaError_t launch_neighbor_query(const int32_t* coords, const HashParams& hp, int32_t* nbr,
@@ -333,6 +503,16 @@ cudaError_t launch_neighbor_query(const int32_t* coords, const HashParams& hp, i
   if (hp.n == 0) return cudaSuccess;
   const int64_t tiles = (hp.n + kTileRows - 1) / kTileRows;
   const int4* c4 = reinterpret_cast<const int4*>(coords);
+  if (hp.k32) {
+    const cudaError_t e =
+        layout == kNbrTileMajor
+            ? launch_dependent(k_neighbor_query32<kNbrTileMajor>, (unsigned)tiles, kTileRows, s,
+                               c4, hp, nbr, tile_mask, pair_count)
+            : launch_dependent(k_neighbor_query32<kNbrRowMajor>, (unsigned)tiles, kTileRows, s,
+                               c4, hp, nbr, tile_mask, pair_count);
+    if (e == cudaSuccess) note_launches(1);
+    return e;
+  }
   const dim3 grid((unsigned)tiles, 9);
   if (layout == kNbrTileMajor) {
     if (hp.k32)

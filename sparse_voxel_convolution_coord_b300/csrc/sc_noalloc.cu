@@ -99,9 +99,10 @@ extern "C" SC_API sc_status sc_build_neighbor_table_noalloc(const int32_t* coord
   const int64_t ntiles = (n + sc::kTileRows - 1) / sc::kTileRows;
   // As sc_build_map: a batch index beyond the 32-bit key space is retried
   // once with 64-bit keys.
-  uint32_t host_local[sc::kStatusBlockBytes / 4] = {};
-  uint32_t* host = sc::status_readback_buffer();
-  if (!host) host = host_local;
+  // The status block comes back into this stack array: pageable memory, so
+  // nothing is allocated (a pinned buffer would need cudaHostAlloc, and the
+  // call synchronises anyway).
+  uint32_t host[sc::kStatusBlockBytes / 4] = {};
   for (int attempt = 0; attempt < 2; ++attempt) {
     e = sc::launch_map_init(hp, tile_mask, ntiles, status, s);
     if (e == cudaSuccess) e = sc::launch_hash_insert(coords, hp, status, s);

@@ -116,3 +116,19 @@ def test_header_is_plain_c(lib, tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.startswith("1 2 2 ")
+
+
+def test_noalloc_source_calls_no_allocator():
+    """The allocation-free entry point's file calls no allocating routine
+    (comments aside): its scratch is the static device array, its status
+    read-back a stack buffer."""
+    import os
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = open(os.path.join(root, "sparse_voxel_convolution_coord_b300", "csrc",
+                            "sc_noalloc.cu")).read()
+    code = re.sub(r"//[^\n]*", "", src)
+    for name in ("cudaMalloc", "cudaHostAlloc", "cudaMallocHost", "cudaFree",
+                 "status_readback_buffer", "new ", "malloc("):
+        assert name not in code, name
+    assert "static __device__ __align__(256)" in code

@@ -1,19 +1,22 @@
-"""The N > 1 path of bench.py on CPU: two gloo ranks on 127.0.0.1.
+"""bench.py's host-side logic, on CPU.
 
-The hot path does not shard across GPUs in this library (replicas only): each
-rank runs the whole workload on its own GPU, ranks meet at a barrier around
-the timed steps, the step time is the maximum over ranks, and the reported
-rate is all ranks' units over that time.  These host-side pieces are what a
-multi-GPU run adds, and they run here without a GPU.
+The path runs on one GPU: our arm refuses more than one (it prints one
+"unavailable" line from rank 0 and exits 0, since the tensor-core kernel's
+weight multicast within a CTA pair is kept to single-GPU runs), and the
+reference arm (the CPU oracle) runs on rank 0 alone.  Both are checked under a
+real two-process launch (torch.distributed.run on 127.0.0.1), which needs no
+GPU.  The rest covers the CPU-baseline leg, the roofline choice and the clock
+record.
 """
+import json
 import os
 import socket
+import subprocess
+import sys
 
 import pytest
 
 torch = pytest.importorskip("torch")
-import torch.distributed as dist  # noqa: E402
-import torch.multiprocessing as mp  # noqa: E402
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -24,48 +27,38 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _rank_main(rank, world, port, results):
-    import sys
-    sys.path.insert(0, ROOT)
-    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
-                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
-    import bench
-    r, w, local = bench.dist_env()
-    d = bench.init_dist(w)
-    try:
-        bench.barrier(d)
-        # each rank reports its own step time; the job takes the slowest
-        t_ms = 1.0 + rank            # rank 0: 1 ms, rank 1: 2 ms
-        t_max = bench.max_over_ranks(d, t_ms)
-        rate = bench.whole_job_rate(w, 1000.0, t_max)
-        bench.barrier(d)
-        results[rank] = (r, w, local, t_max, rate)
-    finally:
-        dist.destroy_process_group()
+def _json_lines(text):
+    return [json.loads(ln) for ln in text.splitlines() if ln.startswith("{")]
 
 
-def test_two_gloo_ranks_max_time_and_whole_job_rate():
-    world = 2
-    ctx = mp.get_context("spawn")
-    with ctx.Manager() as mgr:
-        results = mgr.dict()
-        mp.start_processes(_rank_main, args=(world, _free_port(), results), nprocs=world,
-                           join=True, start_method="spawn")
-        got = dict(results)
-    assert sorted(got) == [0, 1]
-    for rank, (r, w, local, t_max, rate) in got.items():
-        assert (r, w, local) == (rank, world, rank)
-        assert t_max == pytest.approx(2.0)                    # the slowest rank
-        assert rate == pytest.approx(2 * 1000.0 / 2.0e-3)     # all ranks' units / max time
+def test_more_than_one_gpu_is_refused():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2",
+                        "--steps", "3", "--warmup", "3"], capture_output=True, text=True,
+                       timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1 and lines[0]["n_gpus"] == 2
+    assert "multicast" in lines[0]["unavailable"]
 
 
-def test_single_rank_needs_no_process_group():
-    import sys
-    sys.path.insert(0, ROOT)
-    import bench
-    assert bench.init_dist(1) is None
-    assert bench.max_over_ranks(None, 3.5) == 3.5
-    assert bench.whole_job_rate(1, 10.0, 5.0) == pytest.approx(2000.0)
+@pytest.mark.parametrize("impl", ["ours", "reference"])
+def test_two_process_launch(impl):
+    """Under a two-rank launcher: rank 0 prints exactly one line (the refusal
+    for our arm, the CPU oracle's line for the reference arm), rank 1 nothing,
+    and both exit 0."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           os.path.join(ROOT, "bench.py"), "--gpus", "2", "--steps", "3", "--warmup", "3",
+           "--impl", impl, "--config", "1"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stdout + r.stderr
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1, r.stdout
+    if impl == "ours":
+        assert "unavailable" in lines[0]
+    else:
+        assert lines[0]["impl"] == "reference" and lines[0]["value"] > 0
+        assert lines[0]["cpu_baseline"]["kind"] == "oracle"
 
 
 def test_cpu_baseline_reports_all_cores_and_one_thread():

@@ -192,13 +192,18 @@ def test_double_free_is_caught(sc):
 # convolution
 
 def check_problem(sc, coords, res, feats, weight, bias, dtype, rows=None, what=""):
+    """The GPU map equals the oracle's bit for bit, and the GPU convolution
+    matches the oracle's convolution over the ORACLE's map (nothing the
+    reference computes comes from the CUDA path)."""
     m, nbr = gpu_map(sc, coords, res)
+    want = oracle.build_neighbor_table(coords, res)
+    np.testing.assert_array_equal(nbr, want)
     got = gpu_conv(sc, m, feats, weight, bias, dtype)
     if rows is None:
-        ref = oracle.conv(nbr, feats, weight, bias)
+        ref = oracle.conv(want, feats, weight, bias)
         rel = assert_close(got, ref, dtype, what)
     else:
-        ref = oracle.conv(nbr[rows], feats, weight, bias)
+        ref = oracle.conv(want[rows], feats, weight, bias)
         rel = assert_close(got[rows], ref, dtype, what)
     m.free()
     return rel
@@ -450,6 +455,8 @@ def test_fused_epilogue_split_shapes(sc, act, odt):
     tout = TORCH_DT[odt]
     r = _residual(p.n, cout, odt, 7)
     m, nbr = gpu_map(sc, p.coords, p.res)
+    want = oracle.build_neighbor_table(p.coords, p.res)
+    np.testing.assert_array_equal(nbr, want)
     out = sc.sc_forward_ex(m, to_dev(p.feats, torch.bfloat16), to_dev(p.weight, torch.bfloat16),
                            to_dev(p.bias), residual=to_dev(r, tout), act=act, out_dtype=tout)
     sc.sc_device_status(m)
@@ -459,8 +466,36 @@ def test_fused_epilogue_split_shapes(sc, act, odt):
     rows = np.unique(np.concatenate([np.arange(0, 256), np.arange(p.n - 2000, p.n),
                                      rng.choice(p.n, size=2000, replace=False)]))
     acts = {"none": oracle.ACT_NONE, "relu": oracle.ACT_RELU, "silu": oracle.ACT_SILU}
-    ref = oracle.epilogue(oracle.conv(nbr[rows], p.feats, p.weight, p.bias), acts[act], r[rows])
+    ref = oracle.epilogue(oracle.conv(want[rows], p.feats, p.weight, p.bias), acts[act], r[rows])
     check_epilogue_out(got[rows], ref, odt, "bf16", "split %s %s" % (act, odt))
+
+
+@pytest.mark.parametrize("odt", ["f32", "bf16"])
+def test_in_place_residual(sc, odt):
+    """residual == out (an in-place skip connection) at 64^3, C=256, whose
+    last partial round of tiles is split when the output is fp32 and there is
+    no activation: the library runs it unsplit, so every row reads its
+    residual before writing it.  Compared on the first tile, the last 2,000
+    rows (the split tail) and 2,000 random rows."""
+    p = synth.make_problem(3)
+    cout = p.weight.shape[2]
+    tout = TORCH_DT[odt]
+    r = _residual(p.n, cout, odt, 8)
+    m, _ = gpu_map(sc, p.coords, p.res)
+    buf = to_dev(r, tout)
+    got_t = sc.sc_forward_ex(m, to_dev(p.feats, torch.bfloat16), to_dev(p.weight, torch.bfloat16),
+                             to_dev(p.bias), residual=buf, act="none", out_dtype=tout, out=buf)
+    assert got_t.data_ptr() == buf.data_ptr()
+    sc.sc_device_status(m)
+    got = buf.float().cpu().numpy().astype(np.float64)
+    m.free()
+    rng = np.random.default_rng(34)
+    rows = np.unique(np.concatenate([np.arange(0, 128), np.arange(p.n - 2000, p.n),
+                                     rng.choice(p.n, size=2000, replace=False)]))
+    want = oracle.build_neighbor_table(p.coords, p.res)
+    ref = oracle.epilogue(oracle.conv(want[rows], p.feats, p.weight, p.bias), oracle.ACT_NONE,
+                          r[rows])
+    check_epilogue_out(got[rows], ref, odt, "bf16", "in place %s" % odt)
 
 
 def test_forward_ex_rejects_bad_epilogue_arguments(sc):

@@ -96,3 +96,70 @@ def test_noalloc_rejects_beyond_limit_and_reports_errors(lib):
     dup = torch.tensor([[0, 1, 1, 1], [0, 1, 1, 1]], dtype=torch.int32, device="cuda")
     rc, _, _ = noalloc_table(lib, dup, 4)
     assert rc == sc.SC_ERR_DUPLICATE
+
+
+_FRESH_PROCESS = r"""
+import ctypes, json, sys, threading
+import numpy as np
+import torch
+sys.path.insert(0, sys.argv[1])
+import sparse_voxel_convolution_coord_b300 as sc
+from sparse_voxel_convolution_coord_b300 import synth
+
+lib = sc.load_library()
+lib.sc_build_neighbor_table_noalloc.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+p = synth.make_problem(2)
+coords = torch.from_numpy(p.coords).cuda()
+outs = [torch.full((p.n, 27), 7, dtype=torch.int32, device="cuda") for _ in range(2)]
+torch.cuda.synchronize()
+got = {}
+
+
+def call(i):
+    pairs = ctypes.c_int64(-1)
+    got[i] = (lib.sc_build_neighbor_table_noalloc(ctypes.c_void_p(coords.data_ptr()), p.n, p.res,
+                                                  ctypes.c_void_p(outs[i].data_ptr()),
+                                                  ctypes.byref(pairs), None), pairs.value)
+
+
+# the first call into the library in this process, from a thread that never called it
+t = threading.Thread(target=call, args=(0,))
+t.start()
+t.join()
+torch.cuda.synchronize()
+# a second call, from another fresh thread, with the device's free memory read around it
+free0 = torch.cuda.mem_get_info()[0]
+t = threading.Thread(target=call, args=(1,))
+t.start()
+t.join()
+torch.cuda.synchronize()
+free1 = torch.cuda.mem_get_info()[0]
+m = sc.sc_build_map(coords, p.res)
+want = sc.sc_get_neighbor_table(m).cpu().numpy()
+print(json.dumps({"rc": [got[0][0], got[1][0]], "pairs": [got[0][1], got[1][1]],
+                  "want_pairs": m.pairs, "free": [free0, free1],
+                  "equal": [bool(np.array_equal(o.cpu().numpy(), want)) for o in outs]}))
+m.free()
+"""
+
+
+def test_noalloc_first_call_from_a_fresh_thread_of_a_fresh_process(lib):
+    """In a new process, the first call into the library is the no-alloc entry,
+    made from a new host thread: its table equals the allocating path's.  A
+    second call from another new thread leaves the device's free memory
+    unchanged (no allocation on the device), and the status read-back uses the
+    calling thread's stack (no pinned host buffer)."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FRESH_PROCESS, root], capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    assert d["rc"] == [0, 0]
+    assert d["equal"] == [True, True]
+    assert d["pairs"] == [d["want_pairs"]] * 2
+    assert d["free"][0] == d["free"][1]
