@@ -205,6 +205,24 @@ SC_API sc_status sc_forward_ex(sc_handle h, const void* feats, const void* weigh
                                void* stream);
 
 /*
+ * Reorder the map's rows for the convolutions that follow (call once after
+ * the build, on a stream ordered after it; asynchronous).  A 128-row tile
+ * skips an offset only when none of its rows has that neighbour, and in
+ * input order almost every tile holds all 27.  This call sorts the rows by
+ * their 27-bit neighbour-presence masks (stable) and keeps a permuted copy
+ * of the neighbour table with each position's original row, so that tiles
+ * group rows of one neighbourhood shape and skip more offsets (fewer
+ * gathered rows and tensor-core stages); the convolution still writes every
+ * output to its own row, so results are those of the unordered map up to
+ * fp32 summation order.  Costs 112 bytes a row of device memory and a few
+ * kernels; sc_get_neighbor_table and sc_get_pairs are unaffected.  The
+ * pages build the table once per level and reuse it across that level's
+ * convolutions; this is a one-off cost of the same kind (no counterpart on
+ * the pages).  SC_OK, SC_ERR_BAD_HANDLE, SC_ERR_ALLOC or SC_ERR_CUDA.
+ */
+SC_API sc_status sc_map_order_rows(sc_handle h, void* stream);
+
+/*
  * Release a map (library plumbing: the pages have no counterpart; they keep
  * maps in a per-tensor cache).  Its device memory is freed in stream order on `stream`:
  * the caller must order every other stream that used the map before that
@@ -429,6 +447,46 @@ SC_API sc_status sc_level_device_status(sc_level_handle h, void* stream);
 
 /* Release a level map (stream-ordered, as sc_free_map). */
 SC_API sc_status sc_free_level_map(sc_level_handle h, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Dual-grid mesh extraction over a built map ("Running TRELLIS.2 on a Mac
+ * (1/3)", Mesh extraction paragraph: a dual voxel grid, coordinate-to-index
+ * tables, the connected voxels of each edge, quads split into triangles by
+ * how well their normals align; "Porting TRELLIS.2 From Python to Rust and
+ * Metal", results: a compact hash map and a parallel loop).  Readings:
+ * voxel (x, y, z) is the cell [x, x+1] x [y, y+1] x [z, z+1] and owns the
+ * three primal edges from its min corner along +x, +y, +z; flag bit a (0..2)
+ * says its a-edge crosses the surface, bit 3 + a that the edge's start point
+ * is inside.
+ */
+
+/*
+ * Quads of the crossing edges: the voxels at offsets 0, -e_b, -e_b - e_c,
+ * -e_c from the edge's owner ((a, b, c) cyclic), when all four are active,
+ * in that order (right-hand normal along +a for cell-centre vertices),
+ * reversed when the start point is outside.  Listed by owner row, then axis.
+ *   flags   device uint8 [n] (6 bits per voxel, n = sc_map_size).
+ *   quads   device int32 [capacity][4] of voxel rows, 16-byte aligned;
+ *           capacity 3n always suffices.
+ *   q_out   host: receives the number of quads Q.
+ * The four rows of each edge come from the map's neighbour table.
+ * Synchronises `stream` once.
+ */
+SC_API sc_status sc_dual_mesh_quads(sc_handle h, const uint8_t* flags, int32_t* quads,
+                                    int64_t* q_out, void* stream);
+
+/*
+ * Two triangles per quad (q0, q1, q2, q3): (q0, q1, q2), (q0, q2, q3) when
+ * that split's unit normals have the larger dot product, else (q0, q1, q3),
+ * (q1, q2, q3); a tie keeps the first.  Computed in fp64, each product and
+ * sum rounded separately.
+ *   quads     device int32 [nq][4] (16-byte aligned), rows into vertices.
+ *   vertices  device fp32 [n][3]: each voxel's dual vertex.
+ *   tris      device int32 [2 nq][3].
+ * Asynchronous on `stream`.
+ */
+SC_API sc_status sc_dual_mesh_triangulate(const int32_t* quads, int64_t nq, const float* vertices,
+                                          int32_t* tris, void* stream);
 
 /*
  * Cap, for testing the hash's bounded probe loop, on the slots one key's

@@ -28,7 +28,8 @@ __all__ = [
     "sc_build_neighbor_table_noalloc", "sc_build_map_async", "sc_map_status",
     "LevelMap", "sc_subdivide", "sc_channel_to_spatial", "sc_build_level_map",
     "sc_level_parents", "sc_get_level_map", "sc_conv_down", "sc_conv_up",
-    "sc_level_device_status", "sc_free_level_map",
+    "sc_level_device_status", "sc_free_level_map", "sc_dual_mesh_quads",
+    "sc_dual_mesh_triangulate", "sc_map_order_rows",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -124,6 +125,12 @@ def load_library():
     lib.sc_level_device_status.restype = ctypes.c_int
     lib.sc_free_level_map.argtypes = [P, P]
     lib.sc_free_level_map.restype = ctypes.c_int
+    lib.sc_map_order_rows.argtypes = [P, P]
+    lib.sc_map_order_rows.restype = ctypes.c_int
+    lib.sc_dual_mesh_quads.argtypes = [P, P, P, P, P]
+    lib.sc_dual_mesh_quads.restype = ctypes.c_int
+    lib.sc_dual_mesh_triangulate.argtypes = [P, I64, P, P, P]
+    lib.sc_dual_mesh_triangulate.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -262,6 +269,12 @@ def sc_build_map_async(coords, res: int, nbatch: int, stream=None) -> Map:
 def sc_map_status(m: Map) -> None:
     """Wait for the map's build and raise its error, if any."""
     _check(load_library().sc_map_status(ctypes.c_void_p(m.ptr)))
+
+
+def sc_map_order_rows(m: Map, stream=None) -> None:
+    """Sort the map's rows by neighbour mask for the convolutions that follow
+    (outputs still land in their own rows)."""
+    _check(load_library().sc_map_order_rows(ctypes.c_void_p(m.ptr), _stream_ptr(stream)))
 
 
 def sc_free_map(m: Map, stream=None):
@@ -555,3 +568,34 @@ def sc_free_level_map(lm: LevelMap, stream=None):
     rc = load_library().sc_free_level_map(ctypes.c_void_p(lm.ptr), _stream_ptr(stream))
     lm.ptr = 0
     _check(rc)
+
+
+# ---------------------------------------------------------------------------
+# dual-grid mesh
+
+
+def sc_dual_mesh_quads(m: Map, flags, stream=None):
+    """int32 [Q,4] voxel rows of the quads of the map's flagged edges
+    (flags uint8 [N], 6 bits per voxel)."""
+    import torch
+    if flags.dtype != torch.uint8 or flags.numel() != m.n:
+        raise ValueError("flags must be uint8 [N]")
+    quads = torch.empty((max(3 * m.n, 1), 4), dtype=torch.int32, device=m.device)
+    q = ctypes.c_int64(0)
+    _check(load_library().sc_dual_mesh_quads(ctypes.c_void_p(m.ptr), _dev_ptr(flags, "flags"),
+                                             _dev_ptr(quads, "quads"), ctypes.byref(q),
+                                             _stream_ptr(stream)))
+    return quads[:int(q.value)]
+
+
+def sc_dual_mesh_triangulate(quads, vertices, stream=None):
+    """int32 [2Q,3] triangles of quads [Q,4] over fp32 vertices [N,3]."""
+    import torch
+    if vertices.dtype != torch.float32 or vertices.dim() != 2 or vertices.shape[1] != 3:
+        raise ValueError("vertices must be fp32 [N,3]")
+    nq = quads.shape[0]
+    tris = torch.empty((max(2 * nq, 1), 3), dtype=torch.int32, device=quads.device)
+    _check(load_library().sc_dual_mesh_triangulate(_dev_ptr(quads, "quads"), nq,
+                                                   _dev_ptr(vertices, "vertices"),
+                                                   _dev_ptr(tris, "tris"), _stream_ptr(stream)))
+    return tris[:2 * nq]

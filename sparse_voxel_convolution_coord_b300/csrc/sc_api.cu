@@ -141,6 +141,11 @@ void dev_free(H* m, void* p, cudaStream_t s) {
 }
 
 void release_buffers(sc_map* m, cudaStream_t s) {
+  dev_free(m, m->ord_block, s);
+  m->ord_block = nullptr;
+  m->ord_nbr = nullptr;
+  m->ord_mask = nullptr;
+  m->ord_row = nullptr;
   dev_free(m, m->block, s);
   m->block = nullptr;
   m->hash.slots = nullptr;
@@ -567,6 +572,39 @@ sc_status sc_free_map(sc_handle h, void* stream) {
   return ok();
 }
 
+sc_status sc_map_order_rows(sc_handle h, void* stream) {
+  const char* who = "sc_map_order_rows";
+  if (!is_live(h)) return fail(SC_ERR_BAD_HANDLE, "%s: handle is not live", who);
+  if (h->n == 0 || h->ord_block) return ok();
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto up = [](size_t b) { return (b + 255) & ~size_t(255); };
+  const size_t b_nbr = up((size_t)h->ntiles * sc::kTileRows * sc::kTaps * 4);
+  const size_t b_mask = up((size_t)h->ntiles * 4);
+  const size_t b_row = up((size_t)h->ntiles * sc::kTileRows * 4);
+  void* blk = dev_alloc(h, b_nbr + b_mask + b_row, s);
+  void* scratch = blk ? dev_alloc(h, sc::order_scratch_bytes(h->n), s) : nullptr;
+  if (!scratch) {
+    if (blk) dev_free(h, blk, s);
+    return fail(SC_ERR_ALLOC, "%s: device allocation failed", who);
+  }
+  uint8_t* b = static_cast<uint8_t*>(blk);
+  h->ord_block = blk;
+  h->ord_nbr = reinterpret_cast<int32_t*>(b);
+  h->ord_mask = reinterpret_cast<uint32_t*>(b + b_nbr);
+  h->ord_row = reinterpret_cast<int32_t*>(b + b_nbr + b_mask);
+  const cudaError_t e = sc::launch_order_rows(h, scratch, s);
+  dev_free(h, scratch, s);
+  if (e != cudaSuccess) {
+    dev_free(h, blk, s);
+    h->ord_block = nullptr;
+    h->ord_nbr = nullptr;
+    h->ord_mask = nullptr;
+    h->ord_row = nullptr;
+    return fail_cuda(e, who);
+  }
+  return ok();
+}
+
 int64_t sc_map_size(sc_handle h) {
   if (!is_live(h)) {
     fail(SC_ERR_BAD_HANDLE, "sc_map_size: handle is not live");
@@ -876,6 +914,53 @@ sc_status sc_free_level_map(sc_level_handle h, void* stream) {
   if (h->block) dev_free(h, h->block, static_cast<cudaStream_t>(stream));
   h->magic = 0;
   delete h;
+  return ok();
+}
+
+// ---------------------------------------------------------------------------
+// dual-grid mesh
+
+sc_status sc_dual_mesh_quads(sc_handle h, const uint8_t* flags, int32_t* quads, int64_t* q_out,
+                             void* stream) {
+  const char* who = "sc_dual_mesh_quads";
+  if (!is_live(h)) return fail(SC_ERR_BAD_HANDLE, "%s: handle is not live", who);
+  if (!q_out) return fail(SC_ERR_INVALID_ARG, "%s: q_out is NULL", who);
+  *q_out = 0;
+  if (h->n == 0) return ok();
+  if (!flags || !quads || !aligned(quads, 16))
+    return fail(SC_ERR_INVALID_ARG, "%s: flags and a 16-byte aligned quads are required", who);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto up = [](size_t b) { return (b + 255) & ~size_t(255); };
+  const size_t b_cnt = up((size_t)h->n * 4);
+  void* blk = dev_alloc(h, 2 * b_cnt + up(sc::scan_scratch_bytes(h->n)) + 256, s);
+  if (!blk) return fail(SC_ERR_ALLOC, "%s: scratch allocation failed", who);
+  uint8_t* b = static_cast<uint8_t*>(blk);
+  int32_t* counts = reinterpret_cast<int32_t*>(b);
+  int32_t* first = reinterpret_cast<int32_t*>(b + b_cnt);
+  int64_t* total = reinterpret_cast<int64_t*>(b + 2 * b_cnt + up(sc::scan_scratch_bytes(h->n)));
+  int64_t nq = 0;
+  cudaError_t e = sc::launch_quad_counts(h, flags, counts, s);
+  if (e == cudaSuccess)
+    e = sc::scan_exclusive(counts, first, h->n, total, b + 2 * b_cnt, s);
+  if (e == cudaSuccess) e = sc::launch_quads(h, flags, first, quads, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&nq, total, 8, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  dev_free(h, blk, s);
+  if (e != cudaSuccess) return fail_cuda(e, who);
+  *q_out = nq;
+  return ok();
+}
+
+sc_status sc_dual_mesh_triangulate(const int32_t* quads, int64_t nq, const float* vertices,
+                                   int32_t* tris, void* stream) {
+  const char* who = "sc_dual_mesh_triangulate";
+  if (nq < 0) return fail(SC_ERR_INVALID_ARG, "%s: nq < 0", who);
+  if (nq == 0) return ok();
+  if (!quads || !vertices || !tris || !aligned(quads, 16))
+    return fail(SC_ERR_INVALID_ARG, "%s: NULL or unaligned argument", who);
+  const cudaError_t e =
+      sc::launch_triangulate(quads, nq, vertices, tris, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, who);
   return ok();
 }
 

@@ -273,6 +273,21 @@ __global__ void __launch_bounds__(256) k_zero_rows(float4* __restrict__ p, int64
     p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// The same for the rows of positions [pos0, n) through a row indirection
+// (c4 = cout / 4 float4 per row).
+__global__ void __launch_bounds__(256) k_zero_rows_of(float4* __restrict__ out,
+                                                      const int32_t* __restrict__ row_of,
+                                                      int64_t pos0, int64_t n, int c4) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int64_t total = (n - pos0) * c4;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int64_t pos = pos0 + i / c4;
+    const int32_t row = __ldg(row_of + pos);
+    if (row >= 0) out[(int64_t)row * c4 + i % c4] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
 // FUSED: the epilogue applies an activation, adds a residual or rounds to
 // bf16 (the plain variant only adds the bias and stores fp32).
 template <int NPAD, int CS, int CL, bool FUSED>
@@ -803,13 +818,14 @@ struct LaunchCache {
 
 // Cluster size for the weight multicast.  Default: pairs when a W slice has
 // at least two 64-column boxes to split (cout > 64), single CTAs otherwise.
-// SC_CONV_CLUSTER=1|2 overrides it.
+// SC_CONV_CLUSTER=1|2|4 overrides it (4 only where a slice has four boxes).
 int cluster_size(int npad) {
   static int forced = [] {
     const char* e = std::getenv("SC_CONV_CLUSTER");
     const int v = e ? std::atoi(e) : 0;
-    return (v == 1 || v == 2) ? v : 0;
+    return (v == 1 || v == 2 || v == 4) ? v : 0;
   }();
+  if (forced == 4) return npad >= 256 ? 4 : 2;
   if (forced) return forced;
   return npad > 64 ? 2 : 1;
 }
@@ -920,9 +936,7 @@ cudaError_t launch_typed(const ConvMap& m, const void* feats, const void* w, boo
   // An activation or a 16-bit output cannot be applied to partial sums.  In
   // place (residual == out), the split rows would be zeroed, and other parts'
   // sums added, before the last part reads the residual from them.
-  // With a row indirection the split rows are not one range to zero.
-  const bool unsplit =
-      ep.act || ep.out_half || (ep.residual && ep.residual == ep.out) || m.row_of != nullptr;
+  const bool unsplit = ep.act || ep.out_half || (ep.residual && ep.residual == ep.out);
   const int split = unsplit ? 1 : tail_split(nunits, max_clusters, max_stages);
   a.split = split;
   a.tail = split > 1 ? (nunits >= max_clusters ? nunits % max_clusters : nunits) : 0;
@@ -932,11 +946,15 @@ cudaError_t launch_typed(const ConvMap& m, const void* feats, const void* w, boo
   if (a.tail > 0) {
     // The split units' rows start at zero; their parts add into them.  The
     // convolution is this launch's programmatic dependent (attribute 1).
-    const int64_t row0 = a.whole * CL * kTileRows;
-    const int64_t n4 = (m.n - row0) * cout / 4;  // cout is a multiple of 16
+    const int64_t row0 = a.whole * CL * kTileRows;  // first position of the split units
+    const int64_t n4 = (m.n - row0) * cout / 4;     // cout is a multiple of 16
     const int64_t zb = std::min<int64_t>((n4 + 255) / 256, 2 * 148);
-    k_zero_rows<<<(unsigned)zb, 256, 0, s>>>(
-        reinterpret_cast<float4*>(static_cast<float*>(ep.out) + row0 * cout), n4);
+    if (m.row_of)
+      k_zero_rows_of<<<(unsigned)zb, 256, 0, s>>>(static_cast<float4*>(ep.out), m.row_of, row0,
+                                                   m.n, cout / 4);
+    else
+      k_zero_rows<<<(unsigned)zb, 256, 0, s>>>(
+          reinterpret_cast<float4*>(static_cast<float*>(ep.out) + row0 * cout), n4);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     note_launches(1);
@@ -953,6 +971,11 @@ template <int NPAD, int CS>
 cudaError_t launch_cl(const ConvMap& m, const void* feats, const void* w, bool f16,
                       const Epilogue& ep, int cin, int cout, cudaStream_t s) {
   const bool fused = ep.act || ep.residual || ep.out_half;
+  if constexpr (NPAD >= 256) {
+    if (cluster_size(NPAD) == 4)
+      return fused ? launch_typed<NPAD, CS, 4, true>(m, feats, w, f16, ep, cin, cout, s)
+                   : launch_typed<NPAD, CS, 4, false>(m, feats, w, f16, ep, cin, cout, s);
+  }
   if (cluster_size(NPAD) == 2)
     return fused ? launch_typed<NPAD, CS, 2, true>(m, feats, w, f16, ep, cin, cout, s)
                  : launch_typed<NPAD, CS, 2, false>(m, feats, w, f16, ep, cin, cout, s);

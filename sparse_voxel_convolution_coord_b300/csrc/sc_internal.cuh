@@ -417,6 +417,13 @@ struct sc_map {
   int pending;
   cudaEvent_t built;
   uint32_t build_word;
+  // Row order for the convolution (sc_map_order_rows): the tile-major table
+  // over rows sorted by their 27-bit neighbour masks, its tile masks, and
+  // each position's row; nullptr until ordered.
+  void* ord_block;
+  int32_t* ord_nbr;
+  uint32_t* ord_mask;
+  int32_t* ord_row;
 };
 
 namespace sc {
@@ -470,6 +477,11 @@ struct ConvMap {
   uint32_t* status;           // device status word for bounded waits
 };
 inline ConvMap conv_map_of(const sc_map* m) {
+  // Ordered: pad positions (row -1) may sit in any tile, so every position
+  // of every tile is looked at.
+  if (m->ord_nbr)
+    return ConvMap{m->ord_nbr,        m->ord_mask, m->ord_row, m->ntiles * kTileRows,
+                   m->ntiles,         kTaps,       m->d_status};
   return ConvMap{m->nbr, m->tile_mask, nullptr, m->n, m->ntiles, kTaps, m->d_status};
 }
 
@@ -497,10 +509,25 @@ cudaError_t build_level_tables(const int32_t* coords, int64_t n, int res, int nb
                                int32_t* up_row, uint32_t* up_mask, int64_t* np_dev,
                                uint32_t* status, cudaStream_t s);
 cudaError_t launch_child_table(const int32_t* down_nbr, int64_t np, int32_t* out, cudaStream_t s);
+// Dual-grid mesh (sc_mesh.cu).
+cudaError_t launch_quad_counts(const sc_map* m, const uint8_t* flags, int32_t* counts,
+                               cudaStream_t s);
+cudaError_t launch_quads(const sc_map* m, const uint8_t* flags, const int32_t* first,
+                         int32_t* quads, cudaStream_t s);
+cudaError_t launch_triangulate(const int32_t* quads, int64_t nq, const float* verts,
+                               int32_t* tris, cudaStream_t s);
 // sc_sort.cu
 cudaError_t scan_exclusive(const int32_t* in, int32_t* out, int64_t len, int64_t* total,
                            void* scratch, cudaStream_t s);
 size_t scan_scratch_bytes(int64_t len);
+template <typename K>
+cudaError_t sort_pass(const K* keys_in, const int32_t* vals_in, K* keys_out, int32_t* vals_out,
+                      int64_t n, int shift, int bits, void* scratch, cudaStream_t s);
+size_t sort_scratch_bytes(int64_t n, int bins);
+// Row order for the convolution (sc_map.cu): scratch bytes, and the build
+// of m's ord_* tables (allocated by the caller) from its neighbour table.
+size_t order_scratch_bytes(int64_t n);
+cudaError_t launch_order_rows(const sc_map* m, void* scratch, cudaStream_t s);
 
 // Process-wide count of the kernels this library has launched (host side).
 void note_launches(int k);

@@ -20,7 +20,7 @@
 //  the way down    the parents of a voxel set at 2R are the distinct
 //                  (b, x >> 1, y >> 1, z >> 1), in (b, x, y, z) order, each
 //                  with the row of its child o (or -1).  The parents' packed
-//                  keys are radix-sorted with the rows (8-bit stable passes,
+//                  keys are radix-sorted with the rows (9-bit stable passes,
 //                  sc_sort.cu); the first of each run of equal keys starts a
 //                  parent, an exclusive scan of those starts numbers them,
 //                  and a scatter fills the child table (tile-major, as the
@@ -42,15 +42,6 @@
 #include "sc_internal.cuh"
 
 namespace sc {
-
-// sc_sort.cu
-cudaError_t scan_exclusive(const int32_t* in, int32_t* out, int64_t len, int64_t* total,
-                           void* scratch, cudaStream_t s);
-size_t scan_scratch_bytes(int64_t len);
-template <typename K>
-cudaError_t sort_pass(const K* keys_in, const int32_t* vals_in, K* keys_out, int32_t* vals_out,
-                      int64_t n, int shift, int bits, void* scratch, cudaStream_t s);
-size_t sort_scratch_bytes(int64_t n, int bins);
 
 constexpr int kLevelThreads = 256;
 
@@ -259,7 +250,7 @@ size_t level_scratch_bytes(int64_t n, int kbytes) {
   return 2 * up(nn * kbytes) + 2 * up(nn * 4)  // keys, rows (two buffers each)
          + up(nn * 4)                          // octants
          + 2 * up(nn * 4)                      // run starts, their scan
-         + up(std::max(sort_scratch_bytes(n, 256), scan_scratch_bytes(n))) + up(16);
+         + up(std::max(sort_scratch_bytes(n, 512), scan_scratch_bytes(n))) + up(16);
 }
 
 // The way down: fills h's tables from n fine rows; the number of parents is
@@ -300,11 +291,11 @@ cudaError_t build_level_tables(const int32_t* coords, int64_t n, int res, int nb
                                                                           keys[0], octs, status);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // Radix sort of (parent key, row), 8 bits a pass, least significant first
+  // Radix sort of (parent key, row), 9 bits a pass, least significant first
   // (key_bits >= 1, so the rows are always written by a pass).
   int cur = 0;
-  for (int shift = 0; shift < key_bits; shift += 8) {
-    const int bits = std::min(8, key_bits - shift);
+  for (int shift = 0; shift < key_bits; shift += 9) {
+    const int bits = std::min(9, key_bits - shift);
     e = sort_pass<K>(keys[cur], shift == 0 ? nullptr : rows[cur], keys[cur ^ 1], rows[cur ^ 1],
                      n, shift, bits, work, s);
     if (e != cudaSuccess) return e;

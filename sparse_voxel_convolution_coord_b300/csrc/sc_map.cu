@@ -38,6 +38,7 @@
 //  k_pairs_*         CSR pair lists per offset (ascending output row),
 //                    built on demand: count, scan, scatter.
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 
 #include "sc_internal.cuh"
@@ -286,7 +287,7 @@ __global__ void __launch_bounds__(kTileRows) k_neighbor_query(
 // straight out (a warp's stores of one offset are 32 consecutive rows);
 // row-major output is staged in shared memory and written out contiguously.
 template <NbrLayout L>
-__global__ void __launch_bounds__(kTileRows, 8) k_neighbor_query32(
+__global__ void __launch_bounds__(kTileRows, 4) k_neighbor_query32(
     const int4* __restrict__ coords, HashParams hp, int32_t* __restrict__ nbr,
     uint32_t* __restrict__ tile_mask, unsigned long long* pair_count) {
   __shared__ uint32_t s_or[kTileRows / 32];
@@ -320,35 +321,37 @@ __global__ void __launch_bounds__(kTileRows, 8) k_neighbor_query32(
   };
   // The table is written by the insert kernel launched before this one.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // All 26 home slots are loaded before any is looked at, so that the
+  // thread has them all in flight at once.
+  unsigned long long sl[kTaps];
+#pragma unroll
+  for (int k = 0; k < kTaps; ++k) {
+    const int dx = k / 9 - 1, dy = (k / 3) % 3 - 1, dz = k % 3 - 1;
+    const int xx = x + dx, yy = y + dy, zz = z + dz;
+    const bool in = k != kCentre && (unsigned)xx < R && (unsigned)yy < R && (unsigned)zz < R;
+    const uint32_t slot =
+        (((h000 + (uint32_t)((xx >> 1) - bx) * hA + (uint32_t)((yy >> 1) - by) * hB +
+           (uint32_t)((zz >> 1) - bz) * kPhi) >>
+          gshift)
+         << 3) |
+        (uint32_t)(((xx & 1) << 2) | ((yy & 1) << 1) | (zz & 1));
+    sl[k] = in ? __ldg(slots + slot) : kEmptySlot;
+  }
   uint32_t bits = 0, pend = 0;
 #pragma unroll
-  for (int col = 0; col < 9; ++col) {
-    const int dx = col / 3 - 1, dy = col % 3 - 1;
-    const int xx = x + dx, yy = y + dy;
-    const bool colin = (unsigned)xx < R && (unsigned)yy < R;
-    const uint32_t hxy =
-        h000 + (uint32_t)((xx >> 1) - bx) * hA + (uint32_t)((yy >> 1) - by) * hB;
-    const uint32_t cellxy = (uint32_t)(((xx & 1) << 2) | ((yy & 1) << 1));
-    const uint32_t kxy = key0 + (uint32_t)dx * RR + (uint32_t)dy * R;
-#pragma unroll
-    for (int jz = 0; jz < 3; ++jz) {
-      const int k = 3 * col + jz;
-      if (k == kCentre) continue;
-      const int zz = z + jz - 1;
-      const bool in = colin && (unsigned)zz < R;
-      const uint32_t slot = (((hxy + (uint32_t)((zz >> 1) - bz) * kPhi) >> gshift) << 3) |
-                            cellxy | (uint32_t)(zz & 1);
-      const unsigned long long sl = in ? __ldg(slots + slot) : kEmptySlot;
-      int32_t r = -1;
-      if (sl != kEmptySlot) {
-        if ((uint32_t)(sl >> 32) == kxy + (uint32_t)(jz - 1))
-          r = (int32_t)((uint32_t)sl & kRowMask32);
-        else if (sl & kMovedFlag)
-          pend |= 1u << k;
-      }
-      bits |= (r >= 0 ? 1u : 0u) << k;
-      put(k, r);
+  for (int k = 0; k < kTaps; ++k) {
+    if (k == kCentre) continue;
+    const int dx = k / 9 - 1, dy = (k / 3) % 3 - 1, dz = k % 3 - 1;
+    const uint32_t key = key0 + (uint32_t)dx * RR + (uint32_t)dy * R + (uint32_t)dz;
+    int32_t r = -1;
+    if (sl[k] != kEmptySlot) {
+      if ((uint32_t)(sl[k] >> 32) == key)
+        r = (int32_t)((uint32_t)sl[k] & kRowMask32);
+      else if (sl[k] & kMovedFlag)
+        pend |= 1u << k;
     }
+    bits |= (r >= 0 ? 1u : 0u) << k;
+    put(k, r);
   }
   // Lookups that left their home slot: follow the probe sequence.
   const uint32_t cmask = (uint32_t)hp.cap_mask;
@@ -400,6 +403,187 @@ __global__ void __launch_bounds__(kTileRows, 8) k_neighbor_query32(
   if constexpr (L == kNbrRowMajor) {
     // The block's rows [row0, row0 + rows) are one contiguous range of
     // rows * 27 ints: copy it out with 16-byte stores where aligned.
+    const int total = (int)min((int64_t)kTileRows, hp.n - row0) * kTaps;
+    int32_t* dst = nbr + row0 * kTaps;
+    if ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+      const int nvec = total >> 2;
+      for (int i = threadIdx.x; i < nvec; i += kTileRows)
+        reinterpret_cast<int4*>(dst)[i] = reinterpret_cast<const int4*>(s_rows)[i];
+      for (int i = (nvec << 2) + threadIdx.x; i < total; i += kTileRows) dst[i] = s_rows[i];
+    } else {
+      for (int i = threadIdx.x; i < total; i += kTileRows) dst[i] = s_rows[i];
+    }
+  }
+}
+
+// 32-bit keys, staged through shared memory.  A warp loading the home slots
+// of one offset for its 32 voxels touches ~17 different 64-byte groups, so
+// 26 such loads cost ~450 cache-line lookups per warp in L1, which bounds
+// the direct version.  Here each warp first collects the distinct groups of
+// its voxels' 2 x 2 x 2 bricks (one __match_any_sync per brick position),
+// loads each once into shared memory with 16-byte cp.async copies spread
+// over all lanes, and then reads every home slot from shared memory.
+constexpr int kStageEntries = 160;   // groups staged per warp; more fall back to global loads
+constexpr int kStageBytes = 4 * kStageEntries * 64 + 4 * kStageEntries * 4;
+
+template <NbrLayout L>
+__global__ void __launch_bounds__(kTileRows, 4) k_neighbor_query_staged(
+    const int4* __restrict__ coords, HashParams hp, int32_t* __restrict__ nbr,
+    uint32_t* __restrict__ tile_mask, unsigned long long* pair_count) {
+  extern __shared__ __align__(16) uint8_t q_smem[];
+  __shared__ uint32_t s_or[kTileRows / 32];
+  __shared__ uint32_t s_cnt[kTileRows / 32];
+  __shared__ __align__(16) int32_t s_rows[L == kNbrRowMajor ? kTileRows * kTaps : 4];
+  const unsigned long long* slots = reinterpret_cast<const unsigned long long*>(hp.slots);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned long long* groups =
+      reinterpret_cast<unsigned long long*>(q_smem) + warp * (kStageEntries * 8);
+  uint32_t* gids = reinterpret_cast<uint32_t*>(q_smem + 4 * kStageEntries * 64) +
+                   warp * kStageEntries;
+  const int64_t row0 = (int64_t)blockIdx.x * kTileRows;
+  const int64_t o = row0 + threadIdx.x;
+  const bool valid = o < hp.n;
+  const int4 c = valid ? __ldg(coords + o) : make_int4(0, -4, -4, -4);
+  const uint32_t R = (uint32_t)hp.res, BR = (uint32_t)hp.bres;
+  const int x = c.y, y = c.z, z = c.w;
+  const uint32_t key0 = cell_key32(hp, c.x, x, y, z);
+  const int bx = (x - 1) >> 1, by = (y - 1) >> 1, bz = (z - 1) >> 1;
+  const uint32_t brick000 = (((uint32_t)c.x * BR + (uint32_t)bx) * BR + (uint32_t)by) * BR +
+                            (uint32_t)bz;
+  constexpr uint32_t kPhi = 0x9E3779B9u;
+  const uint32_t h000 = brick000 * kPhi, hA = BR * BR * kPhi, hB = BR * kPhi;
+  const int gshift = 32 - (hp.log2cap - 3);
+  const uint32_t RR = R * R;
+  const uint32_t lt = (1u << lane) - 1u;
+  // The table is written by the insert kernel launched before this one.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Distinct groups of the warp, brick position by brick position: ent
+  // holds this lane's entry (8 bits each; 0xff: not staged) per position.
+  uint64_t ent = ~0ull;
+  int nent = 0;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    const int i = b >> 2, j = (b >> 1) & 1, l = b & 1;
+    const bool bv = valid && (uint32_t)(bx + i) < BR && (uint32_t)(by + j) < BR &&
+                    (uint32_t)(bz + l) < BR;
+    const uint32_t g =
+        bv ? ((h000 + (uint32_t)i * hA + (uint32_t)j * hB + (uint32_t)l * kPhi) >> gshift)
+           : 0xffffffffu;
+    const uint32_t peers = __match_any_sync(0xffffffffu, g);
+    const int leader = __ffs(peers) - 1;
+    const bool lead = bv && lane == leader;
+    const uint32_t lm = __ballot_sync(0xffffffffu, lead);
+    const int mine = nent + __popc(lm & lt);
+    if (lead && mine < kStageEntries) gids[mine] = g;
+    const int e = __shfl_sync(0xffffffffu, mine, leader);
+    if (bv && e < kStageEntries) ent &= ~(0xffull << (8 * b)) | ((uint64_t)e << (8 * b));
+    nent += __popc(lm);
+  }
+  nent = min(nent, kStageEntries);
+  __syncwarp();
+  // Entry e's 64 bytes as four 16-byte copies, spread over the lanes.
+  for (int t = lane; t < nent * 4; t += 32) {
+    const int e = t >> 2, q = t & 3;
+    cp_async_16(groups + e * 8 + q * 2, slots + ((uint64_t)gids[e] << 3) + q * 2, 16u);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncwarp();
+
+  int32_t* out_t = nbr + row0 * kTaps + threadIdx.x;
+  int32_t* out_s = s_rows + threadIdx.x * kTaps;
+  auto put = [&](int k, int32_t r) {
+    if constexpr (L == kNbrTileMajor)
+      out_t[k * kTileRows] = r;
+    else
+      out_s[k] = r;
+  };
+  const int px = (x & 1) ^ 1, py = (y & 1) ^ 1, pz = (z & 1) ^ 1;  // brick index of d = 0
+  uint32_t bits = 0, pend = 0;
+#pragma unroll
+  for (int col = 0; col < 9; ++col) {
+    const int dx = col / 3 - 1, dy = col % 3 - 1;
+    const int xx = x + dx, yy = y + dy;
+    const bool colin = (unsigned)xx < R && (unsigned)yy < R;
+    const int i = dx < 0 ? 0 : (dx > 0 ? 1 : px), j = dy < 0 ? 0 : (dy > 0 ? 1 : py);
+    const uint32_t cellxy = (uint32_t)(((xx & 1) << 2) | ((yy & 1) << 1));
+    const uint32_t kxy = key0 + (uint32_t)dx * RR + (uint32_t)dy * R;
+#pragma unroll
+    for (int jz = 0; jz < 3; ++jz) {
+      const int k = 3 * col + jz;
+      if (k == kCentre) continue;
+      const int zz = z + jz - 1;
+      const bool in = colin && (unsigned)zz < R;
+      const int l = jz == 0 ? 0 : (jz == 2 ? 1 : pz);
+      const int b = i * 4 + j * 2 + l;
+      const uint32_t e = (uint32_t)(ent >> (8 * b)) & 0xffu;
+      const uint32_t cell = cellxy | (uint32_t)(zz & 1);
+      unsigned long long sl = kEmptySlot;
+      if (in) {
+        if (e != 0xffu) {
+          sl = groups[e * 8 + cell];
+        } else {
+          const uint32_t g =
+              (h000 + (uint32_t)i * hA + (uint32_t)j * hB + (uint32_t)l * kPhi) >> gshift;
+          sl = __ldg(slots + (((uint64_t)g << 3) | cell));
+        }
+      }
+      int32_t r = -1;
+      if (sl != kEmptySlot) {
+        if ((uint32_t)(sl >> 32) == kxy + (uint32_t)(jz - 1))
+          r = (int32_t)((uint32_t)sl & kRowMask32);
+        else if (sl & kMovedFlag)
+          pend |= 1u << k;
+      }
+      bits |= (r >= 0 ? 1u : 0u) << k;
+      put(k, r);
+    }
+  }
+  // Lookups that left their home slot: follow the probe sequence.
+  const uint32_t cmask = (uint32_t)hp.cap_mask;
+  while (pend) {
+    const int k = __ffs(pend) - 1;
+    pend &= pend - 1u;
+    const int dx = k / 9 - 1, dy = (k / 3) % 3 - 1, dz = k % 3 - 1;
+    const int xx = x + dx, yy = y + dy, zz = z + dz;
+    const uint32_t key = key0 + (uint32_t)dx * RR + (uint32_t)dy * R + (uint32_t)dz;
+    uint32_t pos = (((h000 + (uint32_t)((xx >> 1) - bx) * hA + (uint32_t)((yy >> 1) - by) * hB +
+                      (uint32_t)((zz >> 1) - bz) * kPhi) >>
+                     gshift)
+                    << 3) |
+                   (uint32_t)(((xx & 1) << 2) | ((yy & 1) << 1) | (zz & 1));
+    const uint32_t step = probe_step32(hp, key);
+    for (uint32_t it = 0; it < cmask; ++it) {
+      pos = (pos + step) & cmask;
+      const unsigned long long sl = __ldg(slots + pos);
+      if (sl == kEmptySlot) break;
+      if ((uint32_t)(sl >> 32) == key) {
+        put(k, (int32_t)((uint32_t)sl & kRowMask32));
+        bits |= 1u << k;
+        break;
+      }
+    }
+  }
+  put(kCentre, valid ? (int32_t)o : -1);
+  if (valid) bits |= 1u << kCentre;
+  const uint32_t wor = __reduce_or_sync(0xffffffffu, bits);
+  const uint32_t wcnt = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(bits));
+  if (lane == 0) {
+    s_or[warp] = wor;
+    s_cnt[warp] = wcnt;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t m = 0, bc = 0;
+#pragma unroll
+    for (int w = 0; w < kTileRows / 32; ++w) {
+      m |= s_or[w];
+      bc += s_cnt[w];
+    }
+    tile_mask[blockIdx.x] = m;
+    if (bc) atomicAdd(pair_count + blockIdx.x % kPairCounters, (unsigned long long)bc);
+  }
+  if constexpr (L == kNbrRowMajor) {
     const int total = (int)min((int64_t)kTileRows, hp.n - row0) * kTaps;
     int32_t* dst = nbr + row0 * kTaps;
     if ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
@@ -469,7 +653,7 @@ cudaError_t launch_map_init(const HashParams& hp, uint32_t* tile_mask, int64_t n
 // (griddepcontrol.wait) before it reads that kernel's output.
 template <typename... Params, typename... Args>
 cudaError_t launch_dependent(void (*kern)(Params...), unsigned blocks, unsigned threads,
-                             cudaStream_t s, Args... args) {
+                             size_t smem, cudaStream_t s, Args... args) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -477,6 +661,7 @@ cudaError_t launch_dependent(void (*kern)(Params...), unsigned blocks, unsigned 
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(blocks, 1, 1);
   cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -488,10 +673,10 @@ cudaError_t launch_hash_insert(const int32_t* coords, const HashParams& hp, uint
   if (hp.n == 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((hp.n + kInsertThreads - 1) / kInsertThreads);
   const int4* c4 = reinterpret_cast<const int4*>(coords);
-  cudaError_t e = hp.k32 ? launch_dependent(k_hash_insert<true>, blocks, kInsertThreads, s, c4,
-                                            hp, status)
-                         : launch_dependent(k_hash_insert<false>, blocks, kInsertThreads, s, c4,
-                                            hp, status);
+  cudaError_t e = hp.k32 ? launch_dependent(k_hash_insert<true>, blocks, kInsertThreads, 0, s,
+                                            c4, hp, status)
+                         : launch_dependent(k_hash_insert<false>, blocks, kInsertThreads, 0, s,
+                                            c4, hp, status);
   if (e == cudaSuccess) note_launches(1);
   return e;
 }
@@ -504,12 +689,42 @@ cudaError_t launch_neighbor_query(const int32_t* coords, const HashParams& hp, i
   const int64_t tiles = (hp.n + kTileRows - 1) / kTileRows;
   const int4* c4 = reinterpret_cast<const int4*>(coords);
   if (hp.k32) {
-    const cudaError_t e =
-        layout == kNbrTileMajor
-            ? launch_dependent(k_neighbor_query32<kNbrTileMajor>, (unsigned)tiles, kTileRows, s,
-                               c4, hp, nbr, tile_mask, pair_count)
-            : launch_dependent(k_neighbor_query32<kNbrRowMajor>, (unsigned)tiles, kTileRows, s,
-                               c4, hp, nbr, tile_mask, pair_count);
+    static const int variant = [] {
+      const char* e = std::getenv("SC_QUERY_KERNEL");
+      return e ? std::atoi(e) : 1;
+    }();
+    const int direct = variant == 1;
+    cudaError_t e;
+    if (variant == 0) {
+      const dim3 grid((unsigned)tiles, 9);
+      if (layout == kNbrTileMajor)
+        k_neighbor_query<kNbrTileMajor, true><<<grid, kTileRows, 0, s>>>(c4, hp, nbr, tile_mask,
+                                                                         pair_count);
+      else
+        k_neighbor_query<kNbrRowMajor, true><<<grid, kTileRows, 0, s>>>(c4, hp, nbr, tile_mask,
+                                                                        pair_count);
+      e = cudaGetLastError();
+    } else if (direct) {
+      e = layout == kNbrTileMajor
+              ? launch_dependent(k_neighbor_query32<kNbrTileMajor>, (unsigned)tiles, kTileRows,
+                                 0, s, c4, hp, nbr, tile_mask, pair_count)
+              : launch_dependent(k_neighbor_query32<kNbrRowMajor>, (unsigned)tiles, kTileRows,
+                                 0, s, c4, hp, nbr, tile_mask, pair_count);
+    } else {
+      static bool attr_done = [] {
+        cudaFuncSetAttribute(k_neighbor_query_staged<kNbrTileMajor>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBytes);
+        cudaFuncSetAttribute(k_neighbor_query_staged<kNbrRowMajor>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBytes);
+        return true;
+      }();
+      (void)attr_done;
+      e = layout == kNbrTileMajor
+              ? launch_dependent(k_neighbor_query_staged<kNbrTileMajor>, (unsigned)tiles,
+                                 kTileRows, kStageBytes, s, c4, hp, nbr, tile_mask, pair_count)
+              : launch_dependent(k_neighbor_query_staged<kNbrRowMajor>, (unsigned)tiles,
+                                 kTileRows, kStageBytes, s, c4, hp, nbr, tile_mask, pair_count);
+    }
     if (e == cudaSuccess) note_launches(1);
     return e;
   }
@@ -536,6 +751,143 @@ cudaError_t launch_neighbor_query(const int32_t* coords, const HashParams& hp, i
 cudaError_t launch_nbr_to_row_major(const sc_map* m, int32_t* nbr_out, cudaStream_t s) {
   if (m->n == 0) return cudaSuccess;
   k_nbr_to_row_major<<<(unsigned)m->ntiles, kTileRows, 0, s>>>(m->nbr, m->n, nbr_out);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// row order for the convolution
+//
+// A 128-row tile of the convolution skips an offset only when no row of the
+// tile has that neighbour.  In input order nearly every tile holds every
+// offset (27 per tile against ~15-22 per row on thin shells), so the kernel
+// gathers zero rows for the rest.  Sorting the rows by their 27-bit presence
+// masks (a stable radix sort, least significant 9 bits first) puts rows with
+// the same neighbourhood shape into the same tiles; the permuted tile-major
+// table, its tile masks and each position's original row drive the
+// convolution, whose epilogue writes every position to its row.
+
+__global__ void __launch_bounds__(kTileRows) k_row_masks(const int32_t* __restrict__ nbr_t,
+                                                        int64_t n, uint32_t* __restrict__ masks) {
+  const int64_t o = (int64_t)blockIdx.x * kTileRows + threadIdx.x;
+  if (o >= n) return;
+  const int32_t* col = nbr_t + (int64_t)blockIdx.x * kTileRows * kTaps + threadIdx.x;
+  uint32_t m = 0;
+#pragma unroll
+  for (int k = 0; k < kTaps; ++k) m |= (__ldg(col + k * kTileRows) >= 0 ? 1u : 0u) << k;
+  masks[o] = m;
+}
+
+// One block per output tile: position q takes row perm[q], whose 27 entries
+// are read from a row-major copy of the table (108 contiguous bytes per row;
+// in the tile-major table they would be 27 scattered words) by the lanes of
+// one warp, staged in shared memory, and written out tile-major.
+__global__ void __launch_bounds__(kTileRows) k_permute_table(const int32_t* __restrict__ nbr_rm,
+                                                            const int32_t* __restrict__ perm,
+                                                            int64_t n, int32_t* __restrict__ out_t,
+                                                            uint32_t* __restrict__ out_mask,
+                                                            int32_t* __restrict__ row_of) {
+  __shared__ uint32_t s_or[kTileRows / 32];
+  __shared__ int32_t s_t[kTaps][kTileRows + 1];
+  const int64_t q0 = (int64_t)blockIdx.x * kTileRows;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // warp w copies positions 32w .. 32w + 31, one row (27 lanes) at a time
+  for (int r = 0; r < 32; ++r) {
+    const int pos = warp * 32 + r;
+    const int64_t q = q0 + pos;
+    const int32_t row = q < n ? __ldg(perm + q) : -1;
+    if (lane < kTaps)
+      s_t[lane][pos] = row >= 0 ? __ldg(nbr_rm + (int64_t)row * kTaps + lane) : -1;
+  }
+  __syncthreads();
+  const int64_t q = q0 + threadIdx.x;
+  int32_t* dst = out_t + q0 * kTaps + threadIdx.x;
+  uint32_t bits = 0;
+#pragma unroll
+  for (int k = 0; k < kTaps; ++k) {
+    const int32_t v = s_t[k][threadIdx.x];
+    dst[k * kTileRows] = v;
+    bits |= (v >= 0 ? 1u : 0u) << k;
+  }
+  const int32_t row = q < n ? __ldg(perm + q) : -1;
+  row_of[q] = row;
+  const uint32_t w = __reduce_or_sync(0xffffffffu, bits);
+  if ((threadIdx.x & 31) == 0) s_or[threadIdx.x >> 5] = w;
+  __syncthreads();
+  if (threadIdx.x == 0) out_mask[blockIdx.x] = s_or[0] | s_or[1] | s_or[2] | s_or[3];
+}
+
+// Per tile of the mask-sorted order: 27 - (offsets present in the tile), the
+// key that puts the costliest tiles first.
+__global__ void __launch_bounds__(kTileRows) k_tile_keys(const uint32_t* __restrict__ masks,
+                                                        int64_t n, uint32_t* __restrict__ tkey) {
+  __shared__ uint32_t s_or[kTileRows / 32];
+  const int64_t q = (int64_t)blockIdx.x * kTileRows + threadIdx.x;
+  const uint32_t w = __reduce_or_sync(0xffffffffu, q < n ? __ldg(masks + q) : 0u);
+  if ((threadIdx.x & 31) == 0) s_or[threadIdx.x >> 5] = w;
+  __syncthreads();
+  if (threadIdx.x == 0)
+    tkey[blockIdx.x] = (uint32_t)(kTaps - __popc(s_or[0] | s_or[1] | s_or[2] | s_or[3]));
+}
+
+// Tile j of the final order is tile torder[j] of the mask-sorted one.
+__global__ void __launch_bounds__(kTileRows) k_tile_gather(const int32_t* __restrict__ perm,
+                                                          int64_t n,
+                                                          const int32_t* __restrict__ torder,
+                                                          int32_t* __restrict__ perm2) {
+  const int64_t old = (int64_t)__ldg(torder + blockIdx.x) * kTileRows + threadIdx.x;
+  perm2[(int64_t)blockIdx.x * kTileRows + threadIdx.x] = old < n ? __ldg(perm + old) : -1;
+}
+
+size_t order_scratch_bytes(int64_t n) {
+  auto up = [](size_t b) { return (b + 255) & ~size_t(255); };
+  const size_t ntiles = (size_t)((n + kTileRows - 1) / kTileRows);
+  return 4 * up((size_t)n * 4) + 3 * up(ntiles * 4) + up(ntiles * kTileRows * 4) +
+         std::max(up(sort_scratch_bytes(n, 512)), up((size_t)n * kTaps * 4));
+}
+
+cudaError_t launch_order_rows(const sc_map* m, void* scratch, cudaStream_t s) {
+  auto up = [](size_t b) { return (b + 255) & ~size_t(255); };
+  const int64_t n = m->n;
+  uint8_t* p = static_cast<uint8_t*>(scratch);
+  uint32_t* keys[2] = {reinterpret_cast<uint32_t*>(p),
+                       reinterpret_cast<uint32_t*>(p + up((size_t)n * 4))};
+  int32_t* vals[2] = {reinterpret_cast<int32_t*>(p + 2 * up((size_t)n * 4)),
+                      reinterpret_cast<int32_t*>(p + 3 * up((size_t)n * 4))};
+  const int64_t nt = m->ntiles;
+  uint8_t* p2 = p + 4 * up((size_t)n * 4);
+  uint32_t* tkey = reinterpret_cast<uint32_t*>(p2);
+  uint32_t* tkey_out = reinterpret_cast<uint32_t*>(p2 + up((size_t)nt * 4));
+  int32_t* torder = reinterpret_cast<int32_t*>(p2 + 2 * up((size_t)nt * 4));
+  int32_t* perm2 = reinterpret_cast<int32_t*>(p2 + 3 * up((size_t)nt * 4));
+  void* work = p2 + 3 * up((size_t)nt * 4) + up((size_t)nt * kTileRows * 4);
+  k_row_masks<<<(unsigned)m->ntiles, kTileRows, 0, s>>>(m->nbr, n, keys[0]);
+  note_launches(1);
+  cudaError_t e = cudaGetLastError();
+  int cur = 0;
+  for (int shift = 0; shift < kTaps && e == cudaSuccess; shift += 9) {
+    e = sort_pass<uint32_t>(keys[cur], shift == 0 ? nullptr : vals[cur], keys[cur ^ 1],
+                            vals[cur ^ 1], n, shift, std::min(9, kTaps - shift), work, s);
+    cur ^= 1;
+  }
+  if (e != cudaSuccess) return e;
+  // Tiles with the most offsets first (stable: tiles of one count keep their
+  // mask order), so that the persistent grid's round-robin hands out work
+  // longest first and the last round is made of the cheapest tiles.
+  k_tile_keys<<<(unsigned)nt, kTileRows, 0, s>>>(keys[cur], n, tkey);
+  note_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = sort_pass<uint32_t>(tkey, nullptr, tkey_out, torder, nt, 0, 5, work, s);
+  if (e != cudaSuccess) return e;
+  k_tile_gather<<<(unsigned)nt, kTileRows, 0, s>>>(vals[cur], n, torder, perm2);
+  note_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // The sort's work space is free again: the row-major table goes there.
+  int32_t* nbr_rm = static_cast<int32_t*>(work);
+  e = launch_nbr_to_row_major(m, nbr_rm, s);
+  if (e != cudaSuccess) return e;
+  k_permute_table<<<(unsigned)nt, kTileRows, 0, s>>>(nbr_rm, perm2, nt * kTileRows, m->ord_nbr,
+                                                    m->ord_mask, m->ord_row);
   note_launches(1);
   return cudaGetLastError();
 }

@@ -3,14 +3,14 @@
 // Building blocks of the level-change maps (sc_levels.cu): subdivision needs
 // each parent's first child row (a scan of child counts), the way down needs
 // the distinct parents in (batch, x, y, z) order (a least-significant-digit
-// radix sort of the parents' packed keys, 8 bits per stable pass), and the
+// radix sort of the parents' packed keys, 9 bits per stable pass), and the
 // transposed convolution groups child rows by their octant (one 3-bit pass).
 //
 // Scan: three launches -- per-chunk sums (4096 elements a block), a scan of
 // the chunk sums in one block, and the chunks' own scans with their carry.
 //
 // Counting-sort pass over the digit d = (key >> shift) & (bins - 1), bins <=
-// 256: per-block digit counts [d][block] (digit-major, so that their
+// 512: per-block digit counts [d][block] (digit-major, so that their
 // exclusive scan is each (digit, block)'s first output position), the scan,
 // and a scatter in which every block ranks its elements stably: elements are
 // taken 256 at a time in index order; within a warp __match_any_sync gives
@@ -28,6 +28,7 @@ constexpr int kScanItems = 4;
 constexpr int kScanChunk = kScanThreads * kScanItems;
 
 constexpr int kSortThreads = 256;
+constexpr int kMaxBins = 512;  // digits of up to 9 bits
 constexpr int kSortItems = 8;
 constexpr int kSortTile = kSortThreads * kSortItems;  // elements per block
 
@@ -141,7 +142,7 @@ template <typename K>
 __global__ void __launch_bounds__(kSortThreads) k_digit_counts(const K* __restrict__ keys,
                                                                int64_t n, int shift, int bins,
                                                                int32_t* __restrict__ counts) {
-  __shared__ int32_t s_cnt[256];
+  __shared__ int32_t s_cnt[kMaxBins];
   for (int d = threadIdx.x; d < bins; d += kSortThreads) s_cnt[d] = 0;
   __syncthreads();
   const int64_t base = (int64_t)blockIdx.x * kSortTile;
@@ -160,10 +161,10 @@ __global__ void __launch_bounds__(kSortThreads) k_digit_scatter(
     const K* __restrict__ keys_in, const int32_t* __restrict__ vals_in, int64_t n, int shift,
     int bins, const int32_t* __restrict__ offsets, K* __restrict__ keys_out,
     int32_t* __restrict__ vals_out) {
-  __shared__ int32_t s_wcnt[kSortThreads / 32][256];
-  __shared__ int32_t s_base[256];
+  __shared__ int32_t s_wcnt[kSortThreads / 32][kMaxBins];
+  __shared__ int32_t s_base[kMaxBins];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int d = threadIdx.x; d < 256; d += kSortThreads) {
+  for (int d = threadIdx.x; d < kMaxBins; d += kSortThreads) {
     s_base[d] = d < bins ? offsets[(int64_t)d * gridDim.x + blockIdx.x] : 0;
 #pragma unroll
     for (int w = 0; w < kSortThreads / 32; ++w) s_wcnt[w][d] = 0;

@@ -551,3 +551,80 @@ def test_release_cached_memory_then_rebuild(sc):
     m2, nbr2 = gpu_map(sc, p.coords, p.res)
     np.testing.assert_array_equal(nbr, nbr2)
     m2.free()
+
+
+# ---------------------------------------------------------------------------
+# rows ordered by neighbour mask (sc_map_order_rows): the same results, every
+# output in its own row
+
+@pytest.mark.parametrize("key", [1, 2, 3, 4, 5])
+def test_ordered_rows_match_oracle(sc, key):
+    p = synth.make_problem(key)
+    m, nbr = gpu_map(sc, p.coords, p.res)
+    want = oracle.build_neighbor_table(p.coords, p.res)
+    np.testing.assert_array_equal(nbr, want)
+    sc.sc_map_order_rows(m)
+    # the neighbour table the caller sees is unchanged
+    np.testing.assert_array_equal(sc.sc_get_neighbor_table(m).cpu().numpy(), want)
+    got = gpu_conv(sc, m, p.feats, p.weight, p.bias, p.config.dtype)
+    m.free()
+    rows = None
+    if key in (3, 4):
+        rng = np.random.default_rng(70 + key)
+        rows = np.unique(np.concatenate([np.arange(0, 256), np.arange(p.n - 300, p.n),
+                                         rng.choice(p.n, size=3000, replace=False)]))
+    if rows is None:
+        assert_close(got, oracle.conv(want, p.feats, p.weight, p.bias), p.config.dtype,
+                     "ordered config %d" % key)
+    else:
+        assert_close(got[rows], oracle.conv(want[rows], p.feats, p.weight, p.bias),
+                     p.config.dtype, "ordered config %d" % key)
+
+
+@pytest.mark.parametrize("act,odt,inplace", [("none", "f32", False), ("silu", "bf16", False),
+                                             ("none", "f32", True)])
+def test_ordered_rows_fused_epilogue(sc, act, odt, inplace):
+    """64^3, C=256 over ordered rows: the split tail (zeroed through the row
+    indirection), a fused SiLU with bf16 output, and an in-place residual."""
+    p = synth.make_problem(3)
+    cout = p.weight.shape[2]
+    tout = TORCH_DT[odt]
+    r = _residual(p.n, cout, odt, 9)
+    m, _ = gpu_map(sc, p.coords, p.res)
+    sc.sc_map_order_rows(m)
+    rbuf = to_dev(r, tout)
+    out = sc.sc_forward_ex(m, to_dev(p.feats, torch.bfloat16), to_dev(p.weight, torch.bfloat16),
+                           to_dev(p.bias), residual=rbuf, act=act, out_dtype=tout,
+                           out=rbuf if inplace else None)
+    sc.sc_device_status(m)
+    got = out.float().cpu().numpy().astype(np.float64)
+    m.free()
+    rng = np.random.default_rng(35)
+    rows = np.unique(np.concatenate([np.arange(0, 256), np.arange(p.n - 2000, p.n),
+                                     rng.choice(p.n, size=2000, replace=False)]))
+    want = oracle.build_neighbor_table(p.coords, p.res)
+    acts = {"none": oracle.ACT_NONE, "relu": oracle.ACT_RELU, "silu": oracle.ACT_SILU}
+    ref = oracle.epilogue(oracle.conv(want[rows], p.feats, p.weight, p.bias), acts[act], r[rows])
+    check_epilogue_out(got[rows], ref, odt, "bf16", "ordered %s %s inplace=%s" % (act, odt,
+                                                                                  inplace))
+
+
+def test_ordered_rows_deterministic_and_shuffled(sc):
+    """Shuffled input rows, ordered map, deterministic mode: repeated forwards
+    are bit-identical and equal the oracle's within the bars."""
+    p = synth.make_problem(2)
+    perm = np.random.default_rng(12).permutation(p.n)
+    c, f = np.ascontiguousarray(p.coords[perm]), np.ascontiguousarray(p.feats[perm])
+    m, _ = gpu_map(sc, c, p.res)
+    sc.sc_map_order_rows(m)
+    sc.sc_map_order_rows(m)            # a second call keeps the order
+    sc.sc_set_deterministic(True)
+    try:
+        a = gpu_conv(sc, m, f, p.weight, p.bias, "bf16")
+        b = gpu_conv(sc, m, f, p.weight, p.bias, "bf16")
+    finally:
+        sc.sc_set_deterministic(False)
+    m.free()
+    np.testing.assert_array_equal(a, b)
+    assert_close(a, oracle.conv(oracle.build_neighbor_table(c, p.res), f, p.weight, p.bias),
+                 "bf16", "ordered shuffled")
