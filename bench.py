@@ -300,6 +300,25 @@ def time_forward_alone(sc, torch, m, feats, weight, bias, out, flush, stream, re
     return statistics.median(a.elapsed_time(b) for a, b in evs[10:])
 
 
+def mma_rows_per_pair(nbr, pairs, cl):
+    """Tensor-core rows issued per present (output, neighbour) pair for the
+    map in input order: a unit of `cl` consecutive 128-row tiles runs one
+    stage group per offset present in any of its rows, for all its rows."""
+    n = nbr.shape[0]
+    if n == 0 or pairs == 0:
+        return None
+    tiles = (n + 127) // 128
+    pres = np.zeros((tiles * 128, 27), bool)
+    pres[:n] = nbr >= 0
+    tile_any = pres.reshape(tiles, 128, 27).any(axis=1)
+    units = (tiles + cl - 1) // cl
+    pad = np.zeros((units * cl, 27), bool)
+    pad[:tiles] = tile_any
+    unit_any = pad.reshape(units, cl, 27).any(axis=1)
+    rows_per_unit = np.minimum(cl, tiles - np.arange(units) * cl) * 128
+    return float((unit_any.sum(axis=1) * rows_per_unit).sum() / pairs)
+
+
 def roofline_object(dtype, flops, fwd_bytes, t_kernel_ms, peaks, traffic):
     """The bench line's roofline for one forward launch of t_kernel_ms: the
     tensor pipe or HBM, whichever the algorithmic flops or bytes would take
@@ -466,6 +485,21 @@ def run_ours(args):
         sc.sc_forward(mp, feats, weight, bias, out)
     t_kernel = time_forward_alone(sc, torch, mp, feats, weight, bias, out, flush, stream)
     sc.sc_device_status(mp)
+    mma_rows = mma_rows_per_pair(sc.sc_get_neighbor_table(mp).cpu().numpy(), pairs,
+                                 2 if cout > 64 and p.config.dtype != "f32" else 1)
+    # the same forward over rows ordered by neighbour mask (sc_map_order_rows,
+    # a one-off cost per map), and that cost
+    o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(2e7))
+    o0.record(stream)
+    sc.sc_map_order_rows(mp)
+    o1.record(stream)
+    for _ in range(5):
+        sc.sc_forward(mp, feats, weight, bias, out)
+    t_kernel_ordered = time_forward_alone(sc, torch, mp, feats, weight, bias, out, flush, stream)
+    t_order = o0.elapsed_time(o1)
+    sc.sc_device_status(mp)
     mp.free()
 
     # -- the map build alone: this workload, and the 256^3 ~400k-voxel shells
@@ -542,7 +576,10 @@ def run_ours(args):
         "voxels_per_s": p.n / (t_step * 1e-3),
         "breakdown_ms": {"build_map_in_step": t_build, "forward_in_step": t_fwd,
                          "forward_kernel_alone": t_kernel,
+                         "forward_kernel_alone_rows_ordered": t_kernel_ordered,
+                         "order_rows_once_per_map": t_order,
                          "wall_per_step_incl_flush": wall / K * 1e3},
+        "mma_rows_issued_per_pair": mma_rows,
         "roofline": roofline,
         "map_build": map_build,
         "map_build_256cubed_400k": gate,

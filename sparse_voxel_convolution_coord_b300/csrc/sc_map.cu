@@ -17,24 +17,28 @@
 //                    returns the occupant, so a duplicate key is seen when
 //                    its twin's slot is reached.  Errors are OR-reduced per
 //                    warp.
-//  k_neighbor_query32  (32-bit keys) one thread per voxel: the 27 cells
-//                    around it fall in 2 x 2 x 2 bricks whose group hashes
-//                    follow from one by additions, so all 26 home-slot loads
-//                    are computed at once and issued independently; a lookup
-//                    stops at its home slot on its key, an empty slot, or
-//                    another key whose moved flag is clear, and the few
-//                    others follow their probe sequences afterwards.  The
-//                    tile-major output [tile][27][128] is written coalesced
-//                    (a warp writes 32 consecutive rows of one offset); a
-//                    block is one tile, so it stores the tile's offset mask
-//                    (which the convolution uses to skip absent offsets)
-//                    and adds its pair count to one of 32 global counters.
-//  k_neighbor_query  (64-bit keys) one thread per (voxel, neighbour column
-//                    dx, dy), its three lookups (dz = -1, 0, 1) probing
-//                    until their key or an empty slot.
-//  The insert and the query are launched as programmatic dependents of the
-//  kernel before them: they start while it finishes, read their coordinates,
-//  and wait for it (griddepcontrol.wait) before touching the table.
+//  k_neighbor_query  one thread per (voxel, neighbour column dx, dy): the
+//                    three neighbours dz = -1, 0, 1 of the column are probed
+//                    with three independent loads (brick-local homes put a
+//                    warp's loads, 32 consecutive voxels on one column, on
+//                    few cache lines), collisions followed along the probe
+//                    sequence.  With 32-bit keys a lookup stops at its home
+//                    slot on its key, an empty slot, or another key whose
+//                    moved flag is clear.  The tile-major output
+//                    [tile][27][128] is written coalesced (a warp writes 32
+//                    consecutive rows of one offset).  Each block ORs its
+//                    rows' presence bits into the tile mask the convolution
+//                    uses to skip absent offsets, and adds its pair count to
+//                    one of 32 global counters.  Used up to 2^20 voxels.
+//  k_neighbor_query32  (32-bit keys, 2^20 voxels and more) one thread per
+//                    voxel: the 27 cells around it fall in 2 x 2 x 2 bricks
+//                    whose group hashes follow from one by additions, so all
+//                    26 home-slot loads are issued before any is resolved; a
+//                    block is one tile, so it stores the tile's mask.
+//  The insert, and the per-voxel query, are launched as programmatic
+//  dependents of the kernel before them: they start while it finishes, read
+//  their coordinates, and wait for it (griddepcontrol.wait) before touching
+//  the table.
 //  k_pairs_*         CSR pair lists per offset (ascending output row),
 //                    built on demand: count, scan, scatter.
 #include <algorithm>
@@ -416,187 +420,6 @@ __global__ void __launch_bounds__(kTileRows, 4) k_neighbor_query32(
   }
 }
 
-// 32-bit keys, staged through shared memory.  A warp loading the home slots
-// of one offset for its 32 voxels touches ~17 different 64-byte groups, so
-// 26 such loads cost ~450 cache-line lookups per warp in L1, which bounds
-// the direct version.  Here each warp first collects the distinct groups of
-// its voxels' 2 x 2 x 2 bricks (one __match_any_sync per brick position),
-// loads each once into shared memory with 16-byte cp.async copies spread
-// over all lanes, and then reads every home slot from shared memory.
-constexpr int kStageEntries = 160;   // groups staged per warp; more fall back to global loads
-constexpr int kStageBytes = 4 * kStageEntries * 64 + 4 * kStageEntries * 4;
-
-template <NbrLayout L>
-__global__ void __launch_bounds__(kTileRows, 4) k_neighbor_query_staged(
-    const int4* __restrict__ coords, HashParams hp, int32_t* __restrict__ nbr,
-    uint32_t* __restrict__ tile_mask, unsigned long long* pair_count) {
-  extern __shared__ __align__(16) uint8_t q_smem[];
-  __shared__ uint32_t s_or[kTileRows / 32];
-  __shared__ uint32_t s_cnt[kTileRows / 32];
-  __shared__ __align__(16) int32_t s_rows[L == kNbrRowMajor ? kTileRows * kTaps : 4];
-  const unsigned long long* slots = reinterpret_cast<const unsigned long long*>(hp.slots);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  unsigned long long* groups =
-      reinterpret_cast<unsigned long long*>(q_smem) + warp * (kStageEntries * 8);
-  uint32_t* gids = reinterpret_cast<uint32_t*>(q_smem + 4 * kStageEntries * 64) +
-                   warp * kStageEntries;
-  const int64_t row0 = (int64_t)blockIdx.x * kTileRows;
-  const int64_t o = row0 + threadIdx.x;
-  const bool valid = o < hp.n;
-  const int4 c = valid ? __ldg(coords + o) : make_int4(0, -4, -4, -4);
-  const uint32_t R = (uint32_t)hp.res, BR = (uint32_t)hp.bres;
-  const int x = c.y, y = c.z, z = c.w;
-  const uint32_t key0 = cell_key32(hp, c.x, x, y, z);
-  const int bx = (x - 1) >> 1, by = (y - 1) >> 1, bz = (z - 1) >> 1;
-  const uint32_t brick000 = (((uint32_t)c.x * BR + (uint32_t)bx) * BR + (uint32_t)by) * BR +
-                            (uint32_t)bz;
-  constexpr uint32_t kPhi = 0x9E3779B9u;
-  const uint32_t h000 = brick000 * kPhi, hA = BR * BR * kPhi, hB = BR * kPhi;
-  const int gshift = 32 - (hp.log2cap - 3);
-  const uint32_t RR = R * R;
-  const uint32_t lt = (1u << lane) - 1u;
-  // The table is written by the insert kernel launched before this one.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // Distinct groups of the warp, brick position by brick position: ent
-  // holds this lane's entry (8 bits each; 0xff: not staged) per position.
-  uint64_t ent = ~0ull;
-  int nent = 0;
-#pragma unroll
-  for (int b = 0; b < 8; ++b) {
-    const int i = b >> 2, j = (b >> 1) & 1, l = b & 1;
-    const bool bv = valid && (uint32_t)(bx + i) < BR && (uint32_t)(by + j) < BR &&
-                    (uint32_t)(bz + l) < BR;
-    const uint32_t g =
-        bv ? ((h000 + (uint32_t)i * hA + (uint32_t)j * hB + (uint32_t)l * kPhi) >> gshift)
-           : 0xffffffffu;
-    const uint32_t peers = __match_any_sync(0xffffffffu, g);
-    const int leader = __ffs(peers) - 1;
-    const bool lead = bv && lane == leader;
-    const uint32_t lm = __ballot_sync(0xffffffffu, lead);
-    const int mine = nent + __popc(lm & lt);
-    if (lead && mine < kStageEntries) gids[mine] = g;
-    const int e = __shfl_sync(0xffffffffu, mine, leader);
-    if (bv && e < kStageEntries) ent &= ~(0xffull << (8 * b)) | ((uint64_t)e << (8 * b));
-    nent += __popc(lm);
-  }
-  nent = min(nent, kStageEntries);
-  __syncwarp();
-  // Entry e's 64 bytes as four 16-byte copies, spread over the lanes.
-  for (int t = lane; t < nent * 4; t += 32) {
-    const int e = t >> 2, q = t & 3;
-    cp_async_16(groups + e * 8 + q * 2, slots + ((uint64_t)gids[e] << 3) + q * 2, 16u);
-  }
-  cp_async_commit();
-  cp_async_wait<0>();
-  __syncwarp();
-
-  int32_t* out_t = nbr + row0 * kTaps + threadIdx.x;
-  int32_t* out_s = s_rows + threadIdx.x * kTaps;
-  auto put = [&](int k, int32_t r) {
-    if constexpr (L == kNbrTileMajor)
-      out_t[k * kTileRows] = r;
-    else
-      out_s[k] = r;
-  };
-  const int px = (x & 1) ^ 1, py = (y & 1) ^ 1, pz = (z & 1) ^ 1;  // brick index of d = 0
-  uint32_t bits = 0, pend = 0;
-#pragma unroll
-  for (int col = 0; col < 9; ++col) {
-    const int dx = col / 3 - 1, dy = col % 3 - 1;
-    const int xx = x + dx, yy = y + dy;
-    const bool colin = (unsigned)xx < R && (unsigned)yy < R;
-    const int i = dx < 0 ? 0 : (dx > 0 ? 1 : px), j = dy < 0 ? 0 : (dy > 0 ? 1 : py);
-    const uint32_t cellxy = (uint32_t)(((xx & 1) << 2) | ((yy & 1) << 1));
-    const uint32_t kxy = key0 + (uint32_t)dx * RR + (uint32_t)dy * R;
-#pragma unroll
-    for (int jz = 0; jz < 3; ++jz) {
-      const int k = 3 * col + jz;
-      if (k == kCentre) continue;
-      const int zz = z + jz - 1;
-      const bool in = colin && (unsigned)zz < R;
-      const int l = jz == 0 ? 0 : (jz == 2 ? 1 : pz);
-      const int b = i * 4 + j * 2 + l;
-      const uint32_t e = (uint32_t)(ent >> (8 * b)) & 0xffu;
-      const uint32_t cell = cellxy | (uint32_t)(zz & 1);
-      unsigned long long sl = kEmptySlot;
-      if (in) {
-        if (e != 0xffu) {
-          sl = groups[e * 8 + cell];
-        } else {
-          const uint32_t g =
-              (h000 + (uint32_t)i * hA + (uint32_t)j * hB + (uint32_t)l * kPhi) >> gshift;
-          sl = __ldg(slots + (((uint64_t)g << 3) | cell));
-        }
-      }
-      int32_t r = -1;
-      if (sl != kEmptySlot) {
-        if ((uint32_t)(sl >> 32) == kxy + (uint32_t)(jz - 1))
-          r = (int32_t)((uint32_t)sl & kRowMask32);
-        else if (sl & kMovedFlag)
-          pend |= 1u << k;
-      }
-      bits |= (r >= 0 ? 1u : 0u) << k;
-      put(k, r);
-    }
-  }
-  // Lookups that left their home slot: follow the probe sequence.
-  const uint32_t cmask = (uint32_t)hp.cap_mask;
-  while (pend) {
-    const int k = __ffs(pend) - 1;
-    pend &= pend - 1u;
-    const int dx = k / 9 - 1, dy = (k / 3) % 3 - 1, dz = k % 3 - 1;
-    const int xx = x + dx, yy = y + dy, zz = z + dz;
-    const uint32_t key = key0 + (uint32_t)dx * RR + (uint32_t)dy * R + (uint32_t)dz;
-    uint32_t pos = (((h000 + (uint32_t)((xx >> 1) - bx) * hA + (uint32_t)((yy >> 1) - by) * hB +
-                      (uint32_t)((zz >> 1) - bz) * kPhi) >>
-                     gshift)
-                    << 3) |
-                   (uint32_t)(((xx & 1) << 2) | ((yy & 1) << 1) | (zz & 1));
-    const uint32_t step = probe_step32(hp, key);
-    for (uint32_t it = 0; it < cmask; ++it) {
-      pos = (pos + step) & cmask;
-      const unsigned long long sl = __ldg(slots + pos);
-      if (sl == kEmptySlot) break;
-      if ((uint32_t)(sl >> 32) == key) {
-        put(k, (int32_t)((uint32_t)sl & kRowMask32));
-        bits |= 1u << k;
-        break;
-      }
-    }
-  }
-  put(kCentre, valid ? (int32_t)o : -1);
-  if (valid) bits |= 1u << kCentre;
-  const uint32_t wor = __reduce_or_sync(0xffffffffu, bits);
-  const uint32_t wcnt = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(bits));
-  if (lane == 0) {
-    s_or[warp] = wor;
-    s_cnt[warp] = wcnt;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t m = 0, bc = 0;
-#pragma unroll
-    for (int w = 0; w < kTileRows / 32; ++w) {
-      m |= s_or[w];
-      bc += s_cnt[w];
-    }
-    tile_mask[blockIdx.x] = m;
-    if (bc) atomicAdd(pair_count + blockIdx.x % kPairCounters, (unsigned long long)bc);
-  }
-  if constexpr (L == kNbrRowMajor) {
-    const int total = (int)min((int64_t)kTileRows, hp.n - row0) * kTaps;
-    int32_t* dst = nbr + row0 * kTaps;
-    if ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
-      const int nvec = total >> 2;
-      for (int i = threadIdx.x; i < nvec; i += kTileRows)
-        reinterpret_cast<int4*>(dst)[i] = reinterpret_cast<const int4*>(s_rows)[i];
-      for (int i = (nvec << 2) + threadIdx.x; i < total; i += kTileRows) dst[i] = s_rows[i];
-    } else {
-      for (int i = threadIdx.x; i < total; i += kTileRows) dst[i] = s_rows[i];
-    }
-  }
-}
-
 // nbr_out[n][27] from the tile-major table: one block per tile, staged in
 // shared memory so that both sides are coalesced.
 __global__ void __launch_bounds__(kTileRows) k_nbr_to_row_major(const int32_t* __restrict__ nbr_t,
@@ -689,13 +512,13 @@ cudaError_t launch_neighbor_query(const int32_t* coords, const HashParams& hp, i
   const int64_t tiles = (hp.n + kTileRows - 1) / kTileRows;
   const int4* c4 = reinterpret_cast<const int4*>(coords);
   if (hp.k32) {
-    static const int variant = [] {
-      const char* e = std::getenv("SC_QUERY_KERNEL");
-      return e ? std::atoi(e) : 1;
-    }();
-    const int direct = variant == 1;
+    // Up to ~1M voxels the nine-threads-per-voxel kernel keeps more loads in
+    // flight across the GPU (measured on B300: 17.5 against 20.5 us for a
+    // 30k-voxel build, 49 against 54 us at 400k); beyond, the kernel with
+    // one thread per voxel and all 26 loads in flight is faster (386 against
+    // 457 us at 3.3M).
     cudaError_t e;
-    if (variant == 0) {
+    if (hp.n < (int64_t(1) << 20)) {
       const dim3 grid((unsigned)tiles, 9);
       if (layout == kNbrTileMajor)
         k_neighbor_query<kNbrTileMajor, true><<<grid, kTileRows, 0, s>>>(c4, hp, nbr, tile_mask,
@@ -704,26 +527,12 @@ cudaError_t launch_neighbor_query(const int32_t* coords, const HashParams& hp, i
         k_neighbor_query<kNbrRowMajor, true><<<grid, kTileRows, 0, s>>>(c4, hp, nbr, tile_mask,
                                                                         pair_count);
       e = cudaGetLastError();
-    } else if (direct) {
+    } else {
       e = layout == kNbrTileMajor
               ? launch_dependent(k_neighbor_query32<kNbrTileMajor>, (unsigned)tiles, kTileRows,
                                  0, s, c4, hp, nbr, tile_mask, pair_count)
               : launch_dependent(k_neighbor_query32<kNbrRowMajor>, (unsigned)tiles, kTileRows,
                                  0, s, c4, hp, nbr, tile_mask, pair_count);
-    } else {
-      static bool attr_done = [] {
-        cudaFuncSetAttribute(k_neighbor_query_staged<kNbrTileMajor>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBytes);
-        cudaFuncSetAttribute(k_neighbor_query_staged<kNbrRowMajor>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBytes);
-        return true;
-      }();
-      (void)attr_done;
-      e = layout == kNbrTileMajor
-              ? launch_dependent(k_neighbor_query_staged<kNbrTileMajor>, (unsigned)tiles,
-                                 kTileRows, kStageBytes, s, c4, hp, nbr, tile_mask, pair_count)
-              : launch_dependent(k_neighbor_query_staged<kNbrRowMajor>, (unsigned)tiles,
-                                 kTileRows, kStageBytes, s, c4, hp, nbr, tile_mask, pair_count);
     }
     if (e == cudaSuccess) note_launches(1);
     return e;

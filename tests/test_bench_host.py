@@ -125,3 +125,21 @@ def test_clock_sampler_summary_and_cleanup(tmp_path):
     assert out["sm_mhz"] == 2032 and out["sm_max_mhz"] == 2032 and out["samples"] == 3
     assert out["reasons"] == ["sw_power_cap"]
     assert not os.path.exists(cs.path)
+
+
+def test_mma_rows_per_pair():
+    """Rows the tensor core runs per present pair: 1 when every row of every
+    unit has the unit's offsets; units of two tiles take their union."""
+    import numpy as np
+    import bench
+    nbr = np.zeros((256, 27), np.int32)            # two full tiles: every offset present
+    assert bench.mma_rows_per_pair(nbr, 256 * 27, 1) == 1.0
+    nbr = -np.ones((300, 27), np.int32)            # three tiles (the last ragged)
+    nbr[:, 13] = np.arange(300)                    # centre everywhere
+    nbr[0, 0] = 5                                  # one extra offset in tile 0
+    pairs = 301
+    # cl = 1: tile 0 runs 2 offsets x 128 rows, tiles 1, 2 one offset x 128
+    # (the kernel runs every tile's 128 rows, pad rows included)
+    assert bench.mma_rows_per_pair(nbr, pairs, 1) == (2 * 128 + 128 + 128) / pairs
+    # cl = 2: unit 0 (tiles 0, 1) runs 2 offsets x 256 rows, unit 1 (tile 2) 1 x 128
+    assert bench.mma_rows_per_pair(nbr, pairs, 2) == (2 * 256 + 128) / pairs
