@@ -273,7 +273,7 @@ def run_reference(args):
 # valid only for the kernel source it was measured on (sha1 of the file).
 MEASURED_TRAFFIC = {
     # workload name: (sha1 of sc_conv_tc.cu, bytes per launch)
-    "sq3x64_30k_c256_bf16": ("59f8a28fa8e732fd5411a89ffff1be43c727a8c8", 33268736 + 58624),
+    "sq3x64_30k_c256_bf16": ("9d8a5e5b794ec1a56db8cf38222be037c2645ee6", 33268992 + 94976),
 }
 
 
@@ -355,7 +355,7 @@ def roofline_object(dtype, flops, fwd_bytes, t_kernel_ms, peaks, traffic):
             "tensor_tflops": flops / t_s / 1e12, "algorithmic_bytes_per_launch": fwd_bytes}
 
 
-def time_build(sc, torch, coords, res, flush, stream, reps=60):
+def time_build(sc, torch, coords, res, nbatch, flush, stream, reps=60):
     """Map build timed two ways on the same coordinates, L2 flushed before each:
     device-only (CUDA events around sc_build_map_async: init, insert and query
     kernels, with the stream held by a GPU sleep so host gaps do not count)
@@ -369,7 +369,7 @@ def time_build(sc, torch, coords, res, flush, stream, reps=60):
     for e0, e1 in evs:
         flush.zero_()
         e0.record(stream)
-        maps.append(sc.sc_build_map_async(coords, res, 1))
+        maps.append(sc.sc_build_map_async(coords, res, nbatch))
         e1.record(stream)
     torch.cuda.synchronize()
     sc.sc_map_status(maps[-1])
@@ -505,13 +505,13 @@ def run_ours(args):
     # -- the map build alone: this workload, and the 256^3 ~400k-voxel shells
     # (the largest single build, where the HBM target is set)
     peaks = load_peaks()
-    dev_b, host_b = time_build(sc, torch, coords, p.res, flush, stream)
+    dev_b, host_b = time_build(sc, torch, coords, p.res, nbatch, flush, stream)
     map_build = map_build_object(p.n, dev_b, host_b, peaks, p.config.name)
     gate = None
     if args.config != 5 and not args.no_map_gate:
         p5 = synth.make_problem(5)
         c5 = torch.from_numpy(p5.coords).to(dev)
-        dev5, host5 = time_build(sc, torch, c5, p5.res, flush, stream)
+        dev5, host5 = time_build(sc, torch, c5, p5.res, 1, flush, stream)
         gate = map_build_object(p5.n, dev5, host5, peaks, p5.config.name)
         del c5
 
