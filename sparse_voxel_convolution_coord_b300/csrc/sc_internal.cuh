@@ -139,10 +139,14 @@ inline bool make_hash_params(HashParams& hp, uint64_t* slots, int64_t n, int res
 
 // Host: log2 of the table capacity for n rows, load factor <= 1/4 (a
 // brick's cells share a group of 8 slots; at load 1/2 a third of the
-// lookups of absent neighbours met another key at home).
+// lookups of absent neighbours met another key at home).  The build-time
+// SC_HASH_SLOTS_PER_ROW (default 4) sets the bound.
+#ifndef SC_HASH_SLOTS_PER_ROW
+#define SC_HASH_SLOTS_PER_ROW 4
+#endif
 inline int hash_log2cap(int64_t n) {
   int l = 6;
-  while ((1ull << l) < 4ull * (uint64_t)n) ++l;
+  while ((1ull << l) < (uint64_t)SC_HASH_SLOTS_PER_ROW * (uint64_t)n) ++l;
   return l;
 }
 
@@ -176,8 +180,22 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// SC_TRY_WAIT_HINT_NS (build time, default 0 = the hardware's own limit):
+// how long a try_wait may suspend the thread before it returns false.
+#ifndef SC_TRY_WAIT_HINT_NS
+#define SC_TRY_WAIT_HINT_NS 0
+#endif
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
+#if SC_TRY_WAIT_HINT_NS > 0
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"((uint32_t)SC_TRY_WAIT_HINT_NS)
+      : "memory");
+#else
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -185,6 +203,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
+#endif
   return ok != 0;
 }
 

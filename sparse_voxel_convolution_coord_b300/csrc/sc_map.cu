@@ -151,19 +151,31 @@ __device__ __forceinline__ int32_t finish_probe(const HashParams& hp, uint64_t k
 // Grid (tiles, 9): block (t, col) resolves, for the 128 voxels of tile t,
 // the three neighbours (dz = -1, 0, 1) of neighbour column
 // col = 3 * (dx + 1) + (dy + 1), i.e. offsets k = 3 * col + {0, 1, 2}.
-template <NbrLayout L, bool K32>
+// Grid (tiles, 9 / NCOL): block (t, y) resolves, for the 128 voxels of tile
+// t, the three neighbours (dz = -1, 0, 1) of each of its NCOL neighbour
+// columns col = y * NCOL + i, col = 3 * (dx + 1) + (dy + 1), i.e. offsets
+// k = 3 * col + {0, 1, 2}.  (NCOL > 1 only with 32-bit keys.)
+#ifndef SC_QUERY_NCOL
+#define SC_QUERY_NCOL 1
+#endif
+constexpr int kQueryCols = SC_QUERY_NCOL;
+
+template <NbrLayout L, bool K32, int NCOL = 1>
 __global__ void __launch_bounds__(kTileRows) k_neighbor_query(
     const int4* __restrict__ coords, HashParams hp, int32_t* __restrict__ nbr,
     uint32_t* __restrict__ tile_mask, unsigned long long* pair_count) {
   __shared__ uint32_t s_or[kTileRows / 32];
   __shared__ uint32_t s_cnt[kTileRows / 32];
   const unsigned long long* slots = reinterpret_cast<const unsigned long long*>(hp.slots);
-  const int col = blockIdx.y;
-  const int dx = col / 3 - 1, dy = col % 3 - 1;
   const int64_t row0 = (int64_t)blockIdx.x * kTileRows;
   const int64_t o = row0 + threadIdx.x;
   const bool valid = o < hp.n;
   const int4 c = valid ? __ldg(coords + o) : make_int4(0, 0, 0, 0);
+  uint32_t bits = 0;
+#pragma unroll
+  for (int ci = 0; ci < NCOL; ++ci) {
+  const int col = blockIdx.y * NCOL + ci;
+  const int dx = col / 3 - 1, dy = col % 3 - 1;
   const int x = c.y + dx, y = c.z + dy;
   const bool colin =
       valid && (unsigned)x < (unsigned)hp.res && (unsigned)y < (unsigned)hp.res;
@@ -243,7 +255,6 @@ __global__ void __launch_bounds__(kTileRows) k_neighbor_query(
     for (int j = 0; j < 3; ++j)
       r[j] = in[j] ? finish_probe(hp, key_lo + (uint64_t)j, home[j], sl[j]) : -1;
   }
-  uint32_t bits = 0;
 #pragma unroll
   for (int j = 0; j < 3; ++j) {
     const int k = 3 * col + j;
@@ -253,6 +264,7 @@ __global__ void __launch_bounds__(kTileRows) k_neighbor_query(
       nbr[row0 * kTaps + k * kTileRows + threadIdx.x] = r[j];
     else if (valid)
       nbr[o * kTaps + k] = r[j];
+  }
   }
   const uint32_t cnt = (uint32_t)__popc(bits);
   const int lane = threadIdx.x & 31;
@@ -519,13 +531,13 @@ cudaError_t launch_neighbor_query(const int32_t* coords, const HashParams& hp, i
     // 457 us at 3.3M).
     cudaError_t e;
     if (hp.n < (int64_t(1) << 20)) {
-      const dim3 grid((unsigned)tiles, 9);
+      const dim3 grid((unsigned)tiles, 9 / kQueryCols);
       if (layout == kNbrTileMajor)
-        k_neighbor_query<kNbrTileMajor, true><<<grid, kTileRows, 0, s>>>(c4, hp, nbr, tile_mask,
-                                                                         pair_count);
+        k_neighbor_query<kNbrTileMajor, true, kQueryCols><<<grid, kTileRows, 0, s>>>(
+            c4, hp, nbr, tile_mask, pair_count);
       else
-        k_neighbor_query<kNbrRowMajor, true><<<grid, kTileRows, 0, s>>>(c4, hp, nbr, tile_mask,
-                                                                        pair_count);
+        k_neighbor_query<kNbrRowMajor, true, kQueryCols><<<grid, kTileRows, 0, s>>>(
+            c4, hp, nbr, tile_mask, pair_count);
       e = cudaGetLastError();
     } else {
       e = layout == kNbrTileMajor
