@@ -157,32 +157,44 @@ struct TcArgs {
   int64_t nparts;  // tail * split
   int64_t nitems;  // nparts + whole
   int split;
+  int sv;          // virtual stages per unit (work items are ranges of them)
   int cin;
   int cout;
 };
 
-// Work item i: part `part` of a tail unit (items 0 .. nparts-1, numbered
-// part-major, so a unit's parts go to different clusters and run
-// concurrently), then the whole units (part < 0).
+// A work item: unit `unit`, virtual stage range [a, b) of [0, sv) (the whole
+// unit when a == 0 and b == sv).  A unit of nst real stages runs stages
+// [a nst / sv, b nst / sv): the parts of one unit partition its stages
+// whatever nst is, and the part that ends the unit (b == sv) adds the bias.
 struct WorkItem {
   int64_t unit;
-  int part;
+  int a, b;
 };
-__device__ __forceinline__ WorkItem work_item(const TcArgs& p, int64_t i) {
-  if (i >= p.nparts) return {i - p.nparts, -1};
-  return {p.whole + i % p.tail, (int)(i / p.tail)};
-}
-// Stage range [s0, s1) of an item of a unit with nst stages.  The last part
-// is never empty when nst > 0, so it is the one that adds the bias.
-__device__ __forceinline__ void item_range(const WorkItem& w, int split, int nst, int& s0,
-                                           int& s1) {
-  if (w.part < 0) {
-    s0 = 0;
-    s1 = nst;
-  } else {
-    s0 = (int)((int64_t)w.part * nst / split);
-    s1 = (int)((int64_t)(w.part + 1) * nst / split);
+
+// The items of cluster cid, in order: items cid, cid + ncl, ... of the
+// sequence (tail parts, numbered part-major so that a unit's parts go to
+// different clusters and run concurrently, then the whole units).
+struct ItemIter {
+  int64_t k;
+  __device__ __forceinline__ ItemIter(const TcArgs& p, int64_t cid) : k(cid) {}
+  __device__ __forceinline__ bool next(const TcArgs& p, int64_t ncl, WorkItem& w) {
+    if (k >= p.nitems) return false;
+    if (k >= p.nparts) {
+      w = {k - p.nparts, 0, p.sv};
+    } else {
+      const int part = (int)(k / p.tail);
+      w = {p.whole + k % p.tail, (int)((int64_t)part * p.sv / p.split),
+           (int)((int64_t)(part + 1) * p.sv / p.split)};
+    }
+    k += ncl;
+    return true;
   }
+};
+
+// Stage range [s0, s1) of an item of a unit with nst stages.
+__device__ __forceinline__ void item_range(const WorkItem& w, int sv, int nst, int& s0, int& s1) {
+  s0 = (int)((int64_t)w.a * nst / sv);
+  s1 = (int)((int64_t)w.b * nst / sv);
 }
 
 // Bounded wait with its own limit; ignores the abort flag (used to drain).
@@ -353,11 +365,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t stage = 0, phase = 0, fills = 0;
       int buf = 0;
       bool ok = true;
-      // Refill buffer b with item i's block once every A producer has
-      // released its contents.
-      auto issue_nbr = [&](int64_t i, int b) -> bool {
-        if (i >= p.nitems) return true;
-        const int64_t t = work_item(p, i).unit * CL + rank;
+      // Refill buffer b with item w's block once every A producer has
+      // released its contents (nothing when there is no such item).
+      auto issue_nbr = [&](bool have, const WorkItem& w, int b) -> bool {
+        if (!have) return true;
+        const int64_t t = w.unit * CL + rank;
         if (t >= p.ntiles) return true;
         if ((fills >> (2 + b)) & 1u) {  // used before: wait for the release
           if (!mbar_wait_bounded(&nbr_empty[b], ((fills >> b) & 1u) ^ 1u, abort_flag))
@@ -371,14 +383,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fills |= 1u << (2 + b);  // buffer b used at least once
         return true;
       };
-      ok = issue_nbr(cid, 0);
-      for (int64_t item = cid; item < p.nitems && ok; item += ncl) {
-        const WorkItem wi = work_item(p, item);
+      ItemIter items(p, cid), ahead(p, cid);
+      WorkItem wi, wn;
+      bool have_next = ahead.next(p, ncl, wn);
+      ok = issue_nbr(have_next, wn, 0);
+      while (ok && items.next(p, ncl, wi)) {
+        have_next = ahead.next(p, ncl, wn);  // the item after wi
         const uint32_t mask = unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles);
         int s0, s1;
-        item_range(wi, p.split, unit_stages<CS>(mask, p.cin), s0, s1);
+        item_range(wi, p.sv, unit_stages<CS>(mask, p.cin), s0, s1);
         if constexpr (C::kNbrBufs == 2) {
-          if (!issue_nbr(item + ncl, buf ^ 1)) {
+          if (!issue_nbr(have_next, wn, buf ^ 1)) {
             ok = false;
             break;
           }
@@ -420,7 +435,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // One buffer: the next unit's block as soon as every producer is
         // done with this one (the MMA still holds up to kStages stages).
         if constexpr (C::kNbrBufs == 1) {
-          if (ok && !issue_nbr(item + ncl, 0)) ok = false;
+          if (ok && !issue_nbr(have_next, wn, 0)) ok = false;
         }
         buf ^= C::kNbrBufs - 1;
       }
@@ -451,13 +466,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t stage = 0, phase = 0, nbr_phase = 0;
     int buf = 0;
     bool ok = true;
-    for (int64_t item = cid; item < p.nitems && ok; item += ncl) {
-      const WorkItem wi = work_item(p, item);
+    ItemIter items(p, cid);
+    WorkItem wi;
+    while (ok && items.next(p, ncl, wi)) {
       const int64_t tile = wi.unit * CL + rank;
       const bool has_rows = tile < p.ntiles;
       const uint32_t mask = unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles);
       int s0, s1;
-      item_range(wi, p.split, unit_stages<CS>(mask, p.cin), s0, s1);
+      item_range(wi, p.sv, unit_stages<CS>(mask, p.cin), s0, s1);
       if (has_rows) {
         if (!mbar_wait_bounded(&nbr_full[buf], (nbr_phase >> buf) & 1u, abort_flag)) {
           ok = false;
@@ -528,10 +544,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int64_t item = cid; item < p.nitems && ok; item += ncl) {
-        const WorkItem wi = work_item(p, item);
+      ItemIter items(p, cid);
+      WorkItem wi;
+      while (ok && items.next(p, ncl, wi)) {
         int s0, s1;
-        item_range(wi, p.split, unit_stages<CS>(unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles), p.cin),
+        item_range(wi, p.sv, unit_stages<CS>(unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles), p.cin),
                    s0, s1);
         if (s0 == s1) continue;  // an empty part: no accumulator, no epilogue
         const int nst = s1 - s0;
@@ -586,19 +603,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool ok = true;
     bool rows_zeroed = false;  // the zeroing grid is complete and visible
     const int nchunks = (p.cout + 31) >> 5;
-    for (int64_t item = cid; item < p.nitems && ok; item += ncl) {
-      const WorkItem wi = work_item(p, item);
-      if (wi.part >= 0) {  // a whole unit has rows, so its centre offset: never empty
+    ItemIter items(p, cid);
+    WorkItem wi;
+    while (ok && items.next(p, ncl, wi)) {
+      // Whole units store; parts add into the zeroed rows, the one that ends
+      // the unit with the bias and the residual.  (The host never splits
+      // with an activation or a 16-bit output.)  A whole unit has rows, so
+      // its centre offset: it is never empty; an empty part is skipped, as
+      // the MMA issuer skips it.
+      const bool add = !(wi.a == 0 && wi.b == p.sv);
+      const bool last = wi.b == p.sv;
+      if (add) {
         int s0, s1;
-        item_range(wi, p.split,
+        item_range(wi, p.sv,
                    unit_stages<CS>(unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles), p.cin), s0, s1);
         if (s0 == s1) continue;
       }
-      // Whole units store; parts add into the zeroed rows, the last with the
-      // bias and the residual.  (The host never splits with an activation or
-      // a bf16 output.)
-      const bool add = wi.part >= 0;
-      const bool last = !add || wi.part == p.split - 1;
       const float bscale = last ? 1.f : 0.f;
       const bool resid = FUSED && p.residual != nullptr && last;
       const int64_t wrow0 = (wi.unit * CL + rank) * kTileRows + warp * 32;  // this warp's rows
@@ -846,11 +866,11 @@ int tail_split(int64_t nunits, int64_t G, int max_stages) {
   }();
   const int64_t rem = nunits >= G ? nunits % G : nunits;
   if (rem == 0 || G <= 0) return 1;
+  const double waves = (double)(nunits / G);
+  const double t1 = waves + 1.0;
   // Two addends into a zeroed row sum the same in either order; three do not.
   const int cap = std::max(1, std::min(g_deterministic.load() ? 2 : 8, max_stages / 6));
   if (forced > 0) return std::min(forced, cap);
-  const double waves = (double)(nunits / G);
-  const double t1 = waves + 1.0;
   int best = 1;
   double best_t = t1;
   for (int S = 2; S <= cap; ++S) {
@@ -943,6 +963,7 @@ cudaError_t launch_typed(const ConvMap& m, const void* feats, const void* w, boo
   a.whole = nunits - a.tail;
   a.nparts = a.tail * split;
   a.nitems = a.nparts + a.whole;
+  a.sv = max_stages;
   if (a.tail > 0) {
     // The split units' rows start at zero; their parts add into them.  The
     // convolution is this launch's programmatic dependent (attribute 1).

@@ -63,38 +63,52 @@ __device__ __forceinline__ uint64_t slot_key(const HashParams& hp, unsigned long
     return s >> hp.vbits;
 }
 
-template <bool K32>
+// Voxels per thread of the insert (build-time SC_INSERT_VPT, default 1):
+// more gives each warp independent CAS chains in flight.
+#ifndef SC_INSERT_VPT
+#define SC_INSERT_VPT 1
+#endif
+constexpr int kInsertVpt = SC_INSERT_VPT;
+
+template <bool K32, int VPT = 1>
 __global__ void __launch_bounds__(kInsertThreads) k_hash_insert(const int4* __restrict__ coords,
                                                                 HashParams hp, uint32_t* status) {
   const int lane = threadIdx.x & 31;
-  const int64_t i = (int64_t)blockIdx.x * kInsertThreads + threadIdx.x;
   unsigned long long* slots = reinterpret_cast<unsigned long long*>(hp.slots);
   uint32_t err = 0;
-  bool pending = false;
-  uint64_t key = 0, mine = 0, pos = 0, step = 0, home = 0;
-  if (i < hp.n) {
-    const int4 c = __ldg(coords + i);
-    const bool in_range = c.x >= 0 && (unsigned)c.y < (unsigned)hp.res &&
-                          (unsigned)c.z < (unsigned)hp.res && (unsigned)c.w < (unsigned)hp.res;
-    if (!in_range) {
-      err |= kStatRange;
-    } else if ((uint64_t)c.x >= hp.bmax) {
-      err |= kStatKeySpace;
-    } else if constexpr (K32) {
-      const uint32_t k32 = cell_key32(hp, c.x, c.y, c.z, c.w);
-      key = k32;
-      mine = ((uint64_t)k32 << 32) | (uint64_t)i;
-      pos = home_slot32(hp, c.x, c.y, c.z, c.w);
-      step = probe_step32(hp, k32);
-      pending = true;
-    } else {
-      key = cell_key(hp, c.x, c.y, c.z, c.w);
-      mine = (key << hp.vbits) | (uint64_t)i;
-      pos = home_slot(hp, c.x, c.y, c.z, c.w);
-      step = probe_step(hp, key);
-      pending = true;
+  bool pending[VPT];
+  uint64_t key[VPT], mine[VPT], pos[VPT], step[VPT], home[VPT];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    // voxel v of this thread: blocks cover VPT * kInsertThreads consecutive rows
+    const int64_t i =
+        ((int64_t)blockIdx.x * VPT + v) * kInsertThreads + threadIdx.x;
+    pending[v] = false;
+    key[v] = mine[v] = pos[v] = step[v] = 0;
+    if (i < hp.n) {
+      const int4 c = __ldg(coords + i);
+      const bool in_range = c.x >= 0 && (unsigned)c.y < (unsigned)hp.res &&
+                            (unsigned)c.z < (unsigned)hp.res && (unsigned)c.w < (unsigned)hp.res;
+      if (!in_range) {
+        err |= kStatRange;
+      } else if ((uint64_t)c.x >= hp.bmax) {
+        err |= kStatKeySpace;
+      } else if constexpr (K32) {
+        const uint32_t k32 = cell_key32(hp, c.x, c.y, c.z, c.w);
+        key[v] = k32;
+        mine[v] = ((uint64_t)k32 << 32) | (uint64_t)i;
+        pos[v] = home_slot32(hp, c.x, c.y, c.z, c.w);
+        step[v] = probe_step32(hp, k32);
+        pending[v] = true;
+      } else {
+        key[v] = cell_key(hp, c.x, c.y, c.z, c.w);
+        mine[v] = (key[v] << hp.vbits) | (uint64_t)i;
+        pos[v] = home_slot(hp, c.x, c.y, c.z, c.w);
+        step[v] = probe_step(hp, key[v]);
+        pending[v] = true;
+      }
     }
-    home = pos;
+    home[v] = pos[v];
   }
   // Everything above read only the coordinates; the table is cleared by the
   // kernel launched before this one (a programmatic dependency when launched
@@ -102,24 +116,37 @@ __global__ void __launch_bounds__(kInsertThreads) k_hash_insert(const int4* __re
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // Synchronous probing rounds; at most hp.probe_limit rounds (every slot,
-  // unless sc_set_probe_limit set a smaller cap).
-  for (uint64_t round = 0; __any_sync(0xffffffffu, pending); ++round) {
-    if (!pending) continue;
-    if (round >= hp.probe_limit) {
-      err |= kStatTableFull;
-      pending = false;
-      continue;
+  // unless sc_set_probe_limit set a smaller cap).  A thread's voxels take
+  // their CAS of a round together.
+  auto any_pending = [&]() {
+    bool a = false;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) a |= pending[v];
+    return a;
+  };
+  for (uint64_t round = 0; __any_sync(0xffffffffu, any_pending()); ++round) {
+    unsigned long long old[VPT];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      if (pending[v] && round >= hp.probe_limit) {
+        err |= kStatTableFull;
+        pending[v] = false;
+      }
+      old[v] = pending[v] ? atomicCAS(slots + pos[v], kEmptySlot, mine[v]) : 0ull;
     }
-    const unsigned long long old = atomicCAS(slots + pos, kEmptySlot, mine);
-    if (old == kEmptySlot) {
-      pending = false;
-    } else if (slot_key<K32>(hp, old) == key) {
-      err |= kStatDuplicate;
-      pending = false;
-    } else {
-      // 32-bit keys: mark the home slot, whose key moved on.
-      if (K32 && round == 0) atomicOr(slots + home, (unsigned long long)kMovedFlag);
-      pos = (pos + step) & hp.cap_mask;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      if (!pending[v]) continue;
+      if (old[v] == kEmptySlot) {
+        pending[v] = false;
+      } else if (slot_key<K32>(hp, old[v]) == key[v]) {
+        err |= kStatDuplicate;
+        pending[v] = false;
+      } else {
+        // 32-bit keys: mark the home slot, whose key moved on.
+        if (K32 && round == 0) atomicOr(slots + home[v], (unsigned long long)kMovedFlag);
+        pos[v] = (pos[v] + step[v]) & hp.cap_mask;
+      }
     }
   }
   err = __reduce_or_sync(0xffffffffu, err);
@@ -171,6 +198,9 @@ __global__ void __launch_bounds__(kTileRows) k_neighbor_query(
   const int64_t o = row0 + threadIdx.x;
   const bool valid = o < hp.n;
   const int4 c = valid ? __ldg(coords + o) : make_int4(0, 0, 0, 0);
+  // The table is written by the insert kernel launched before this one (a
+  // programmatic dependency: this grid may start while that one finishes).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   uint32_t bits = 0;
 #pragma unroll
   for (int ci = 0; ci < NCOL; ++ci) {
@@ -503,15 +533,33 @@ cudaError_t launch_dependent(void (*kern)(Params...), unsigned blocks, unsigned 
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Params>(args)...);
 }
 
+// The same with a two-dimensional grid.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent2(void (*kern)(Params...), dim3 grid, unsigned threads,
+                              cudaStream_t s, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Params>(args)...);
+}
+
 cudaError_t launch_hash_insert(const int32_t* coords, const HashParams& hp, uint32_t* status,
                                cudaStream_t s) {
   if (hp.n == 0) return cudaSuccess;
-  const unsigned blocks = (unsigned)((hp.n + kInsertThreads - 1) / kInsertThreads);
+  const int64_t per_block = (int64_t)kInsertThreads * kInsertVpt;
+  const unsigned blocks = (unsigned)((hp.n + per_block - 1) / per_block);
   const int4* c4 = reinterpret_cast<const int4*>(coords);
-  cudaError_t e = hp.k32 ? launch_dependent(k_hash_insert<true>, blocks, kInsertThreads, 0, s,
-                                            c4, hp, status)
-                         : launch_dependent(k_hash_insert<false>, blocks, kInsertThreads, 0, s,
-                                            c4, hp, status);
+  cudaError_t e = hp.k32 ? launch_dependent(k_hash_insert<true, kInsertVpt>, blocks,
+                                            kInsertThreads, 0, s, c4, hp, status)
+                         : launch_dependent(k_hash_insert<false, kInsertVpt>, blocks,
+                                            kInsertThreads, 0, s, c4, hp, status);
   if (e == cudaSuccess) note_launches(1);
   return e;
 }
@@ -532,13 +580,11 @@ cudaError_t launch_neighbor_query(const int32_t* coords, const HashParams& hp, i
     cudaError_t e;
     if (hp.n < (int64_t(1) << 20)) {
       const dim3 grid((unsigned)tiles, 9 / kQueryCols);
-      if (layout == kNbrTileMajor)
-        k_neighbor_query<kNbrTileMajor, true, kQueryCols><<<grid, kTileRows, 0, s>>>(
-            c4, hp, nbr, tile_mask, pair_count);
-      else
-        k_neighbor_query<kNbrRowMajor, true, kQueryCols><<<grid, kTileRows, 0, s>>>(
-            c4, hp, nbr, tile_mask, pair_count);
-      e = cudaGetLastError();
+      e = layout == kNbrTileMajor
+              ? launch_dependent2(k_neighbor_query<kNbrTileMajor, true, kQueryCols>, grid,
+                                  kTileRows, s, c4, hp, nbr, tile_mask, pair_count)
+              : launch_dependent2(k_neighbor_query<kNbrRowMajor, true, kQueryCols>, grid,
+                                  kTileRows, s, c4, hp, nbr, tile_mask, pair_count);
     } else {
       e = layout == kNbrTileMajor
               ? launch_dependent(k_neighbor_query32<kNbrTileMajor>, (unsigned)tiles, kTileRows,
