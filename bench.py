@@ -551,6 +551,57 @@ def run_ours(args):
     torch.cuda.synchronize()
     t_e2e = e0.elapsed_time(e1) / KE
 
+    # The same steps pipelined, as a serving loop would run them: two sets of
+    # device buffers; step i's inputs go up on one copy stream while the
+    # main stream computes step i - 1 and another copy stream brings step
+    # i - 2's result down (PCIe carries both directions at once).  Every
+    # step still copies all its inputs up and its whole result down.
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    dbufs = [(d_coords, d_feats, d_weight, d_bias, out)] + [
+        (torch.empty_like(coords), torch.empty_like(feats), torch.empty_like(weight),
+         torch.empty_like(bias), torch.empty_like(out))]
+    h_outs = [h_out, torch.empty_like(h_out).pin_memory()]
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # step's inputs landed
+    ev_used = [torch.cuda.Event() for _ in range(2)]  # step's compute done with its buffers
+    ev_down = [torch.cuda.Event() for _ in range(2)]  # step's result left the device
+    for ev in ev_in + ev_used + ev_down:
+        ev.record(stream)
+
+    def pipe_step(i):
+        b = i % 2
+        dc, df, dw, db, do = dbufs[b]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_used[b])
+            dc.copy_(h_coords, non_blocking=True)
+            df.copy_(h_feats, non_blocking=True)
+            dw.copy_(h_weight, non_blocking=True)
+            db.copy_(h_bias, non_blocking=True)
+            ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_down[b])
+        mp = sc.sc_build_map_async(dc, p.res, nbatch)
+        sc.sc_forward(mp, df, dw, db, do)
+        ev_used[b].record(stream)
+        mp.free()
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_used[b])
+            h_outs[b].copy_(do, non_blocking=True)
+            ev_down[b].record(s_out)
+
+    for i in range(3):
+        pipe_step(i)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for i in range(KE):
+        pipe_step(i)
+    stream.wait_event(ev_down[(KE - 1) % 2])
+    stream.wait_event(ev_in[(KE - 1) % 2])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e_pipe = e0.elapsed_time(e1) / KE
+
     conv_src = os.path.join(ROOT, "sparse_voxel_convolution_coord_b300", "csrc", "sc_conv_tc.cu")
     traffic = None
     rec = MEASURED_TRAFFIC.get(p.config.name)
@@ -583,8 +634,14 @@ def run_ours(args):
         "roofline": roofline,
         "map_build": map_build,
         "map_build_256cubed_400k": gate,
-        "e2e": {"value": flops / (t_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "ms_per_step": t_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": flops / (t_e2e_pipe * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": t_e2e_pipe, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": KE,
+                "how": "public API (sc_build_map_async + sc_forward) from pinned host buffers; "
+                       "inputs up on one copy stream, result down on another, compute on "
+                       "the main stream, two device buffer sets (steps overlap)",
+                "serial": {"value": flops / (t_e2e * 1e-3) / 1e12, "ms_per_step": t_e2e,
+                           "how": "copy up, build, forward, copy down on one stream"}},
         # counted by the library at each of its launches over the timed steps
         # (map build: init, insert, query; forward: conv, plus the zeroing
         # kernel when a partial last round of tiles is split)

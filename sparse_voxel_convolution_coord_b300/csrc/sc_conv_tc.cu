@@ -90,6 +90,19 @@ namespace sc {
 constexpr int kLoaderWarp = 4;                          // W boxes + neighbour blocks
 constexpr int kProducerWarps = SC_PRODUCER_WARPS;       // A gathers: warps 5 .. 4 + kProducerWarps
 constexpr int kProducerThreads = 32 * kProducerWarps;
+// The producers form groups that take the pipeline stages in turn (stage g
+// of the CTA's sequence goes to group g mod groups), so a thread issues
+// `groups` times the copies of one stage per wait and arrival, with that
+// many stage times to do it.  Four groups where the MMAs of a stage are
+// short (NPAD <= 64), two otherwise (measured on B300); build-time
+// SC_PRODUCER_GROUPS overrides.
+#ifndef SC_PRODUCER_GROUPS
+#define SC_PRODUCER_GROUPS 0
+#endif
+template <int NPAD>
+constexpr int producer_groups() {
+  return SC_PRODUCER_GROUPS > 0 ? SC_PRODUCER_GROUPS : (NPAD <= 64 ? 4 : 2);
+}
 constexpr int kMmaWarp = 5 + kProducerWarps;
 constexpr int kTcThreads = 32 * (kMmaWarp + 1);
 
@@ -109,9 +122,13 @@ struct TcCfg {
   static constexpr int kRowBytes = CS * 2;              // one gathered row segment
   static constexpr int kChunks = kRowBytes / 16;        // 16-byte copies per row segment
   static constexpr int kSegCopies = kTileRows * kChunks;        // 16-byte copies per segment
-  static constexpr int kPerThread = kSegs * kSegCopies / kProducerThreads;
-  static_assert(kPerThread * kProducerThreads == kSegs * kSegCopies &&
-                    kProducerThreads % kChunks == 0,
+  static constexpr int kGroups = producer_groups<NPAD>();
+  static constexpr int kGroupThreads = kProducerThreads / kGroups;
+  static_assert(kGroupThreads * kGroups == kProducerThreads && kGroupThreads % 32 == 0,
+                "producer groups are whole warps");
+  static constexpr int kPerThread = kSegs * kSegCopies / kGroupThreads;
+  static_assert(kPerThread * kGroupThreads == kSegs * kSegCopies &&
+                    kGroupThreads % kChunks == 0,
                 "producer threads must tile the stage's copies");
   static constexpr int kASeg = kTileRows * kRowBytes;   // bytes per A segment
   static constexpr int kABytes = kTileRows * 128;       // 16 KB per stage
@@ -333,7 +350,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&full[s], kProducerThreads + 1);  // one per A producer + the loader's expect_tx
+      mbar_init(&full[s], C::kGroupThreads + 1);  // one per thread of a producer group + the loader
       mbar_init(&empty[s], CL);  // one commit from the MMA warp of every CTA of the cluster
     }
     for (int a = 0; a < 2; ++a) {
@@ -460,10 +477,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else if (warp > kLoaderWarp && warp < kMmaWarp) {
     // ------------------------------------------------------------ A producers
-    const int pt = threadIdx.x - 32 * (kLoaderWarp + 1);  // 0 .. kProducerThreads - 1
+    const int pt0 = threadIdx.x - 32 * (kLoaderWarp + 1);  // 0 .. kProducerThreads - 1
+    const int grp = pt0 / C::kGroupThreads;     // this thread's producer group
+    const int pt = pt0 % C::kGroupThreads;      // its place in the group
     const int chunk_id = pt % C::kChunks;       // which 16 bytes of a row segment
-    const __nv_bfloat16* feats = p.feats;
+    // The stage's kSegs x 128 rows x kChunks 16-byte copies, thread pt of the
+    // group taking copies q = pt + i * kGroupThreads (consecutive threads:
+    // consecutive chunks of one row).  Copy i reads row r_i of segment i *
+    // kGroupThreads / kSegCopies (the segment does not depend on pt, as
+    // kSegCopies is a multiple of kGroupThreads) and lands at byte dst_i
+    // of the stage: row r of a segment starts at r * kRowBytes, and its chunk
+    // c sits at c ^ ((r * kRowBytes >> 7) & (kChunks - 1)) (the 128/64/32-byte
+    // swizzle of the operand descriptors).  All of this is fixed per thread;
+    // a stage only looks up its rows and issues the copies.
+    static_assert(C::kSegCopies % C::kGroupThreads == 0, "a pass of copies stays in one segment");
+    int r_i[C::kPerThread];
+    uint32_t dst_i[C::kPerThread];
+#pragma unroll
+    for (int i = 0; i < C::kPerThread; ++i) {
+      const int q = pt + i * C::kGroupThreads;
+      const int r = (q / C::kChunks) % kTileRows;
+      const int sw = (r * C::kRowBytes >> 7) & (C::kChunks - 1);
+      r_i[i] = r;
+      dst_i[i] = (uint32_t)((i * C::kGroupThreads / C::kSegCopies) * C::kASeg + r * C::kRowBytes +
+                            ((chunk_id ^ sw) << 4));
+    }
+    const char* const fbase = reinterpret_cast<const char*>(p.feats) + chunk_id * 16;
+    const int rstride = p.cin * 2;  // bytes per feature row
     uint32_t stage = 0, phase = 0, nbr_phase = 0;
+    uint32_t gst = 0;  // stages of the CTA's sequence so far (all items)
     int buf = 0;
     bool ok = true;
     ItemIter items(p, cid);
@@ -484,45 +526,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int32_t* nb = s_nbr + buf * (kTileRows * kTaps);
       OffsetIter<CS> it(mask, p.cin, p.taps);
       it.skip(s0);
-      for (int s = s0; s < s1; ++s) {
+      for (int s = s0; s < s1; ++s, ++gst) {
+        int ks[C::kSegs];
+        const int c0 = it.next(ks);
+        if ((int)(gst % C::kGroups) != grp) {  // another group's stage
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          continue;
+        }
         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
         uint8_t* a_st = sA + stage * C::kABytes;
-        int ks[C::kSegs];
-        const int c0 = it.next(ks);
-        // The stage's kSegs x 128 rows x kChunks 16-byte copies, thread pt
-        // taking copies pt, pt + kProducerThreads, ... (consecutive threads:
-        // consecutive chunks of one row).  Row r of a segment starts at
-        // r * kRowBytes; its chunk c lands at c ^ ((r * kRowBytes >> 7) &
-        // (kChunks - 1)) (the 128/64/32-byte swizzle of the operand
-        // descriptors).  Absent neighbours copy a row of zeros.
-        int32_t src_rows[C::kPerThread];
+        // Segment j's offset as a row base in the neighbour block, -1 where
+        // the segment pads the last stage (k == taps) or the tile is past
+        // the end; absent neighbours (-1 in the block) copy zeros (source
+        // size 0 reads nothing: a shared zero row would make every SM hit
+        // the same L2 line).
+        int kb[C::kSegs];
+#pragma unroll
+        for (int jj = 0; jj < C::kSegs; ++jj)
+          kb[jj] = (has_rows && ks[jj] < p.taps) ? ks[jj] * kTileRows : -1;
+        const char* const fsrc = fbase + c0 * 2;
+        // All rows first (their shared-memory loads overlap), then the copies.
+        int row[C::kPerThread];
 #pragma unroll
         for (int i = 0; i < C::kPerThread; ++i) {
-          const int q = pt + i * kProducerThreads;
-          const int j = q / C::kSegCopies;
-          const int r = (q / C::kChunks) % kTileRows;
-          int k = ks[0];
-#pragma unroll
-          for (int jj = 1; jj < C::kSegs; ++jj)
-            if (j == jj) k = ks[jj];
-          src_rows[i] = (has_rows && k < p.taps) ? nb[k * kTileRows + r] : -1;
+          const int j = i * C::kGroupThreads / C::kSegCopies;
+          row[i] = nb[max(kb[j], 0) + r_i[i]];
+          if (kb[j] < 0) row[i] = -1;
         }
 #pragma unroll
-        for (int i = 0; i < C::kPerThread; ++i) {
-          const int q = pt + i * kProducerThreads;
-          const int j = q / C::kSegCopies;
-          const int r = (q / C::kChunks) % kTileRows;
-          const int sw = (r * C::kRowBytes >> 7) & (C::kChunks - 1);
-          uint8_t* dst = a_st + j * C::kASeg + r * C::kRowBytes + ((chunk_id ^ sw) << 4);
-          // Absent neighbours: source size 0 zero-fills without reading (a
-          // shared zero row would make every SM hit the same L2 line).
-          const __nv_bfloat16* src =
-              src_rows[i] >= 0 ? feats + (int64_t)src_rows[i] * p.cin + c0 + chunk_id * 8 : feats;
-          cp_async_16(dst, src, src_rows[i] >= 0 ? 16u : 0u);
-        }
+        for (int i = 0; i < C::kPerThread; ++i)
+          cp_async_16(a_st + dst_i[i], row[i] >= 0 ? fsrc + (int64_t)row[i] * rstride : fbase,
+                      row[i] >= 0 ? 16u : 0u);
         cp_async_arrive_noinc(&full[stage]);
         if (++stage == C::kStages) {
           stage = 0;
@@ -535,7 +575,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (!ok) {
       *s_abort = 1;
-      if (pt == 0) atomicOr(p.status, kStatTimeout);
+      if (pt0 == 0) atomicOr(p.status, kStatTimeout);
     }
     cp_async_wait<0>();
   } else if (warp == kMmaWarp) {
