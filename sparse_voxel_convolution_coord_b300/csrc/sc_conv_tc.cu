@@ -116,6 +116,12 @@ constexpr int kEpiBytes = 4 * 32 * kStageRow * 4;       // 18,432 B
 constexpr uint64_t kWaitNs = 2000000000ull;             // bounded waits: 2 s
 constexpr uint64_t kDrainNs = 50000000ull;              // final drain after an abort: 50 ms
 
+// Ring depth cap (build-time SC_MAX_STAGES); the shared-memory budget sets
+// the depth below it.
+#ifndef SC_MAX_STAGES
+#define SC_MAX_STAGES 8
+#endif
+
 template <int NPAD, int CS>
 struct TcCfg {
   static constexpr int kSegs = 64 / CS;                 // offset segments per stage
@@ -144,12 +150,18 @@ struct TcCfg {
   // kStageRow floats), bias, barriers.
   static constexpr int kFixed = kNbrBufs * kNbrBytes + kEpiBytes + NPAD * 4 + 256;
   static constexpr int kStages0 = (kSmemLimit - 1024 - kFixed) / kStageBytes;
-  static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
+  static constexpr int kStages = kStages0 > SC_MAX_STAGES ? SC_MAX_STAGES : kStages0;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kFixed;
   static constexpr uint32_t kTmemCols = (2 * NPAD <= 128) ? 128 : (2 * NPAD <= 256 ? 256 : 512);
   static constexpr uint32_t kLayoutA = CS == 64 ? 2u : (CS == 32 ? 4u : 6u);
   static constexpr uint32_t kSboA = 8 * kRowBytes;
   static_assert(kStages >= 2, "pipeline needs two stages");
+  // A group waits on a slot's empty barrier by phase parity for the stage
+  // kStages before its own; it has issued its previous stage, kGroups
+  // earlier, so every stage up to kGroups + kStages back has been consumed.
+  // The stage 2 kStages back must be among them, or the slot's barrier may
+  // still be a phase behind and the parity test would pass early.
+  static_assert(kStages >= kGroups, "producer groups need at least one ring slot each");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
 };
 
