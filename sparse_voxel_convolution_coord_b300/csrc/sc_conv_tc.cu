@@ -100,8 +100,8 @@ constexpr int kProducerThreads = 32 * kProducerWarps;
 #define SC_PRODUCER_GROUPS 0
 #endif
 template <int NPAD>
-constexpr int producer_groups() {
-  return SC_PRODUCER_GROUPS > 0 ? SC_PRODUCER_GROUPS : (NPAD <= 64 ? 4 : 2);
+constexpr int producer_groups(int stages) {
+  return SC_PRODUCER_GROUPS > 0 ? SC_PRODUCER_GROUPS : (NPAD <= 64 && stages >= 4 ? 4 : 2);
 }
 constexpr int kMmaWarp = 5 + kProducerWarps;
 constexpr int kTcThreads = 32 * (kMmaWarp + 1);
@@ -122,25 +122,22 @@ constexpr uint64_t kDrainNs = 50000000ull;              // final drain after an 
 #define SC_MAX_STAGES 8
 #endif
 
-template <int NPAD, int CS>
+// SEGS segments of CS channels per stage: one segment (CS = 64) is one
+// offset's 64-channel block of a wide input; several (cin == CS) are that
+// many offsets' whole rows.  64 / CS by default (K = 64 per stage); twice
+// that for the narrow layers, whose stages are otherwise too short for the
+// per-stage synchronisation.
+template <int NPAD, int CS, int SEGS = 64 / CS>
 struct TcCfg {
-  static constexpr int kSegs = 64 / CS;                 // offset segments per stage
+  static constexpr int kSegs = SEGS;                    // segments per stage
+  static constexpr int kKst = SEGS * CS;                // K (channels) per stage
   static constexpr int kRowBytes = CS * 2;              // one gathered row segment
   static constexpr int kChunks = kRowBytes / 16;        // 16-byte copies per row segment
   static constexpr int kSegCopies = kTileRows * kChunks;        // 16-byte copies per segment
-  static constexpr int kGroups = producer_groups<NPAD>();
-  static constexpr int kGroupThreads = kProducerThreads / kGroups;
-  static_assert(kGroupThreads * kGroups == kProducerThreads && kGroupThreads % 32 == 0,
-                "producer groups are whole warps");
-  static constexpr int kPerThread = kSegs * kSegCopies / kGroupThreads;
-  static_assert(kPerThread * kGroupThreads == kSegs * kSegCopies &&
-                    kGroupThreads % kChunks == 0,
-                "producer threads must tile the stage's copies");
   static constexpr int kASeg = kTileRows * kRowBytes;   // bytes per A segment
-  static constexpr int kABytes = kTileRows * 128;       // 16 KB per stage
+  static constexpr int kABytes = kTileRows * kKst * 2;  // 16 or 32 KB per stage
   static constexpr int kBlocksN = NPAD / 64;            // 64-column blocks of B
-  static constexpr int kBBytes = 64 * NPAD * 2;         // 64 K rows x NPAD bf16
-  static constexpr int kBBoxes = kSegs * kBlocksN;      // TMA boxes of B per stage
+  static constexpr int kBBytes = kKst * NPAD * 2;       // kKst K rows x NPAD bf16
   static constexpr int kStageBytes = kABytes + kBBytes;
   // Neighbour blocks: two (the next unit's prefetched during this one) for
   // cout <= 64, whose short units would expose the refill; one otherwise,
@@ -152,10 +149,19 @@ struct TcCfg {
   static constexpr int kStages0 = (kSmemLimit - 1024 - kFixed) / kStageBytes;
   static constexpr int kStages = kStages0 > SC_MAX_STAGES ? SC_MAX_STAGES : kStages0;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kFixed;
+  static constexpr int kGroups = producer_groups<NPAD>(kStages);
+  static constexpr int kGroupThreads = kProducerThreads / kGroups;
+  static_assert(kGroupThreads * kGroups == kProducerThreads && kGroupThreads % 32 == 0,
+                "producer groups are whole warps");
+  static constexpr int kPerThread = kSegs * kSegCopies / kGroupThreads;
+  static_assert(kPerThread * kGroupThreads == kSegs * kSegCopies &&
+                    kGroupThreads % kChunks == 0,
+                "producer threads must tile the stage's copies");
   static constexpr uint32_t kTmemCols = (2 * NPAD <= 128) ? 128 : (2 * NPAD <= 256 ? 256 : 512);
   static constexpr uint32_t kLayoutA = CS == 64 ? 2u : (CS == 32 ? 4u : 6u);
   static constexpr uint32_t kSboA = 8 * kRowBytes;
   static_assert(kStages >= 2, "pipeline needs two stages");
+  static_assert(SEGS > 1 || CS == 64, "a one-segment stage is a 64-channel block");
   // A group waits on a slot's empty barrier by phase parity for the stage
   // kStages before its own; it has issued its previous stage, kGroups
   // earlier, so every stage up to kGroups + kStages back has been consumed.
@@ -248,25 +254,24 @@ __device__ __forceinline__ uint32_t unit_mask(const uint32_t* tile_mask, int64_t
   return m;
 }
 
-// Stages of a unit: (present offsets) x (cin / 64) when CS == 64, else the
-// present offsets taken 64/CS at a time.
-template <int CS>
+// Stages of a unit: (present offsets) x (cin / 64) with one segment per
+// stage, else the present offsets taken SEGS at a time.
+template <int CS, int SEGS>
 __device__ __forceinline__ int unit_stages(uint32_t mask, int cin) {
   const int np = __popc(mask);
-  if constexpr (CS == 64) {
+  if constexpr (SEGS == 1) {
     return np * (cin >> 6);
   } else {
-    constexpr int g = 64 / CS;
-    return (np + g - 1) / g;
+    return (np + SEGS - 1) / SEGS;
   }
 }
 
-// Walks the K slices of a unit in order: for CS == 64, each present offset
-// k (ascending) with its cin/64 channel blocks; for CS < 64, the present
-// offsets 64/CS at a time (k = taps, one past the last offset, pads the last
-// stage: its W box lies past the end of W and is zero-filled).  next() fills
-// the stage's offsets and returns its first channel.
-template <int CS>
+// Walks the K slices of a unit in order: with one segment per stage, each
+// present offset k (ascending) with its cin/64 channel blocks; otherwise the
+// present offsets SEGS at a time (k = taps, one past the last offset, pads
+// the last stage: its W box lies past the end of W and is zero-filled).
+// next() fills the stage's offsets and returns its first channel.
+template <int CS, int SEGS>
 struct OffsetIter {
   uint32_t rem;
   int cblk = 0, cblocks, taps;
@@ -274,18 +279,18 @@ struct OffsetIter {
       : rem(mask), cblocks(cin >> 6), taps(taps_) {}
   // Step over the first `n` stages.
   __device__ __forceinline__ void skip(int n) {
-    if constexpr (CS == 64) {
+    if constexpr (SEGS == 1) {
       cblk += n;
       while (cblk >= cblocks) {
         cblk -= cblocks;
         rem &= rem - 1u;
       }
     } else {
-      for (int i = 0; i < n * (64 / CS); ++i) rem &= rem - 1u;
+      for (int i = 0; i < n * SEGS; ++i) rem &= rem - 1u;
     }
   }
-  __device__ __forceinline__ int next(int (&ks)[64 / CS]) {
-    if constexpr (CS == 64) {
+  __device__ __forceinline__ int next(int (&ks)[SEGS]) {
+    if constexpr (SEGS == 1) {
       ks[0] = __ffs(rem) - 1;
       const int c0 = cblk * 64;
       if (++cblk == cblocks) {
@@ -295,7 +300,7 @@ struct OffsetIter {
       return c0;
     } else {
 #pragma unroll
-      for (int j = 0; j < 64 / CS; ++j) {
+      for (int j = 0; j < SEGS; ++j) {
         ks[j] = rem ? __ffs(rem) - 1 : taps;
         rem &= rem - 1u;
       }
@@ -331,10 +336,10 @@ __global__ void __launch_bounds__(256) k_zero_rows_of(float4* __restrict__ out,
 
 // FUSED: the epilogue applies an activation, adds a residual or rounds to
 // bf16 (the plain variant only adds the bias and stores fp32).
-template <int NPAD, int CS, int CL, bool FUSED>
+template <int NPAD, int CS, int SEGS, int CL, bool FUSED>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_conv_tc(const __grid_constant__ CUtensorMap tm_b, const TcArgs p) {
-  using C = TcCfg<NPAD, CS>;
+  using C = TcCfg<NPAD, CS, SEGS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -420,14 +425,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         have_next = ahead.next(p, ncl, wn);  // the item after wi
         const uint32_t mask = unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles);
         int s0, s1;
-        item_range(wi, p.sv, unit_stages<CS>(mask, p.cin), s0, s1);
+        item_range(wi, p.sv, unit_stages<CS, SEGS>(mask, p.cin), s0, s1);
         if constexpr (C::kNbrBufs == 2) {
           if (!issue_nbr(have_next, wn, buf ^ 1)) {
             ok = false;
             break;
           }
         }
-        OffsetIter<CS> it(mask, p.cin, p.taps);
+        OffsetIter<CS, SEGS> it(mask, p.cin, p.taps);
         it.skip(s0);
         for (int s = s0; s < s1; ++s) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
@@ -447,7 +452,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const int b = j * C::kBlocksN + nb2;
               if ((uint32_t)(b % CL) == rank) {
                 // k == 27 addresses rows past W's end: the box is zero-filled.
-                uint8_t* dst = b_st + nb2 * (64 * 128) + j * CS * 128;
+                uint8_t* dst = b_st + nb2 * (C::kKst * 128) + j * CS * 128;
                 const int32_t y = ks[j] * p.cin + c0;
                 if constexpr (CL > 1)
                   tma_load_2d_multicast(dst, &tm_b, &full[stage], nb2 * 64, y, kAllCtas);
@@ -527,7 +532,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool has_rows = tile < p.ntiles;
       const uint32_t mask = unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles);
       int s0, s1;
-      item_range(wi, p.sv, unit_stages<CS>(mask, p.cin), s0, s1);
+      item_range(wi, p.sv, unit_stages<CS, SEGS>(mask, p.cin), s0, s1);
       if (has_rows) {
         if (!mbar_wait_bounded(&nbr_full[buf], (nbr_phase >> buf) & 1u, abort_flag)) {
           ok = false;
@@ -536,7 +541,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         nbr_phase ^= 1u << buf;
       }
       const int32_t* nb = s_nbr + buf * (kTileRows * kTaps);
-      OffsetIter<CS> it(mask, p.cin, p.taps);
+      OffsetIter<CS, SEGS> it(mask, p.cin, p.taps);
       it.skip(s0);
       for (int s = s0; s < s1; ++s, ++gst) {
         int ks[C::kSegs];
@@ -596,11 +601,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
+      // Operand descriptors of stage 0, segment 0, K step 0.
+      const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, C::kSboA, C::kLayoutA);
+      const uint64_t b_desc0 = smem_desc(smem_u32(sB), C::kKst * 128, 1024, 2u);
       ItemIter items(p, cid);
       WorkItem wi;
       while (ok && items.next(p, ncl, wi)) {
         int s0, s1;
-        item_range(wi, p.sv, unit_stages<CS>(unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles), p.cin),
+        item_range(wi, p.sv, unit_stages<CS, SEGS>(unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles), p.cin),
                    s0, s1);
         if (s0 == s1) continue;  // an empty part: no accumulator, no epilogue
         const int nst = s1 - s0;
@@ -617,15 +625,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           tc_fence_after();
           fence_proxy_async_smem();  // the A rows were written by cp.async (generic proxy)
-          const uint32_t a_base = smem_u32(sA + stage * C::kABytes);
-          const uint32_t b_base = smem_u32(sB + stage * C::kBBytes);
+          // The stage's descriptors differ from stage 0's only in the start
+          // address field (bits 0-13, address / 16; every operand address
+          // stays below 256 KB, so the field never carries).
+          const uint64_t ad_s = a_desc0 + (uint64_t)((stage * C::kABytes) >> 4);
+          const uint64_t bd_s = b_desc0 + (uint64_t)((stage * C::kBBytes) >> 4);
 #pragma unroll
           for (int j = 0; j < C::kSegs; ++j) {
 #pragma unroll
             for (int kk = 0; kk < CS / 16; ++kk) {
-              const uint64_t ad =
-                  smem_desc(a_base + j * C::kASeg + kk * 32, 16, C::kSboA, C::kLayoutA);
-              const uint64_t bd = smem_desc(b_base + (j * CS + kk * 16) * 128, 64 * 128, 1024, 2u);
+              const uint64_t ad = ad_s + (uint64_t)((j * C::kASeg + kk * 32) >> 4);
+              const uint64_t bd = bd_s + (uint64_t)(((j * CS + kk * 16) * 128) >> 4);
               tc_mma_bf16(d_tmem, ad, bd, p.idesc, (s | j | kk) != 0 ? 1u : 0u);
             }
           }
@@ -668,7 +678,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (add) {
         int s0, s1;
         item_range(wi, p.sv,
-                   unit_stages<CS>(unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles), p.cin), s0, s1);
+                   unit_stages<CS, SEGS>(unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles), p.cin), s0, s1);
         if (s0 == s1) continue;
       }
       const float bscale = last ? 1.f : 0.f;
@@ -935,11 +945,11 @@ int tail_split(int64_t nunits, int64_t G, int max_stages) {
   return best_t < 0.95 * t1 ? best : 1;
 }
 
-template <int NPAD, int CS, int CL, bool FUSED>
+template <int NPAD, int CS, int SEGS, int CL, bool FUSED>
 cudaError_t launch_typed(const ConvMap& m, const void* feats, const void* w, bool f16,
                          const Epilogue& ep, int cin, int cout, cudaStream_t s) {
-  using C = TcCfg<NPAD, CS>;
-  auto kern = k_conv_tc<NPAD, CS, CL, FUSED>;
+  using C = TcCfg<NPAD, CS, SEGS>;
+  auto kern = k_conv_tc<NPAD, CS, SEGS, CL, FUSED>;
   static LaunchCache cache;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1004,7 +1014,7 @@ cudaError_t launch_typed(const ConvMap& m, const void* feats, const void* w, boo
   a.cout = cout;
   const int64_t nunits = (m.ntiles + CL - 1) / CL;
   if (nunits == 0) return cudaSuccess;
-  const int max_stages = CS == 64 ? m.taps * (cin / 64) : (m.taps + 64 / CS - 1) / (64 / CS);
+  const int max_stages = SEGS == 1 ? m.taps * (cin / 64) : (m.taps + SEGS - 1) / SEGS;
   // An activation or a 16-bit output cannot be applied to partial sums.  In
   // place (residual == out), the split rows would be zeroed, and other parts'
   // sums added, before the last part reads the residual from them.
@@ -1040,28 +1050,38 @@ cudaError_t launch_typed(const ConvMap& m, const void* feats, const void* w, boo
   return e;
 }
 
-template <int NPAD, int CS>
+template <int NPAD, int CS, int SEGS>
 cudaError_t launch_cl(const ConvMap& m, const void* feats, const void* w, bool f16,
                       const Epilogue& ep, int cin, int cout, cudaStream_t s) {
   const bool fused = ep.act || ep.residual || ep.out_half;
   if constexpr (NPAD >= 256) {
     if (cluster_size(NPAD) == 4)
-      return fused ? launch_typed<NPAD, CS, 4, true>(m, feats, w, f16, ep, cin, cout, s)
-                   : launch_typed<NPAD, CS, 4, false>(m, feats, w, f16, ep, cin, cout, s);
+      return fused ? launch_typed<NPAD, CS, SEGS, 4, true>(m, feats, w, f16, ep, cin, cout, s)
+                   : launch_typed<NPAD, CS, SEGS, 4, false>(m, feats, w, f16, ep, cin, cout, s);
   }
   if (cluster_size(NPAD) == 2)
-    return fused ? launch_typed<NPAD, CS, 2, true>(m, feats, w, f16, ep, cin, cout, s)
-                 : launch_typed<NPAD, CS, 2, false>(m, feats, w, f16, ep, cin, cout, s);
-  return fused ? launch_typed<NPAD, CS, 1, true>(m, feats, w, f16, ep, cin, cout, s)
-               : launch_typed<NPAD, CS, 1, false>(m, feats, w, f16, ep, cin, cout, s);
+    return fused ? launch_typed<NPAD, CS, SEGS, 2, true>(m, feats, w, f16, ep, cin, cout, s)
+                 : launch_typed<NPAD, CS, SEGS, 2, false>(m, feats, w, f16, ep, cin, cout, s);
+  return fused ? launch_typed<NPAD, CS, SEGS, 1, true>(m, feats, w, f16, ep, cin, cout, s)
+               : launch_typed<NPAD, CS, SEGS, 1, false>(m, feats, w, f16, ep, cin, cout, s);
 }
+
+// Wide stages for narrow layers (build-time SC_NARROW_K128, default on).
+#ifndef SC_NARROW_K128
+#define SC_NARROW_K128 1
+#endif
+constexpr bool kNarrowStages = SC_NARROW_K128 != 0;
 
 template <int NPAD>
 cudaError_t launch_npad(const ConvMap& m, const void* feats, const void* w, bool f16,
                         const Epilogue& ep, int cin, int cout, cudaStream_t s) {
-  if (cin == 16) return launch_cl<NPAD, 16>(m, feats, w, f16, ep, cin, cout, s);
-  if (cin == 32) return launch_cl<NPAD, 32>(m, feats, w, f16, ep, cin, cout, s);
-  return launch_cl<NPAD, 64>(m, feats, w, f16, ep, cin, cout, s);
+  // Narrow layers (cout <= 64, cin <= 64): K = 128 per stage, so that each
+  // stage's fixed synchronisation cost is spread over eight MMAs.
+  constexpr int W = (NPAD <= 64 && kNarrowStages) ? 2 : 1;
+  if (cin == 16) return launch_cl<NPAD, 16, 4 * W>(m, feats, w, f16, ep, cin, cout, s);
+  if (cin == 32) return launch_cl<NPAD, 32, 2 * W>(m, feats, w, f16, ep, cin, cout, s);
+  if (cin == 64) return launch_cl<NPAD, 64, W>(m, feats, w, f16, ep, cin, cout, s);
+  return launch_cl<NPAD, 64, 1>(m, feats, w, f16, ep, cin, cout, s);
 }
 
 }  // namespace
