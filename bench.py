@@ -273,7 +273,7 @@ def run_reference(args):
 # valid only for the kernel source it was measured on (sha1 of the file).
 MEASURED_TRAFFIC = {
     # workload name: (sha1 of sc_conv_tc.cu, bytes per launch)
-    "sq3x64_30k_c256_bf16": ("9d8a5e5b794ec1a56db8cf38222be037c2645ee6", 33268992 + 94976),
+    "sq3x64_30k_c256_bf16": ("8ed9b41d29bd2d809f8807ee808422dc0e0ce5d3", 33279744 + 46080),
 }
 
 
