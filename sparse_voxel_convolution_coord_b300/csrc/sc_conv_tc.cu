@@ -254,24 +254,27 @@ __device__ __forceinline__ uint32_t unit_mask(const uint32_t* tile_mask, int64_t
   return m;
 }
 
-// Stages of a unit: (present offsets) x (cin / 64) with one segment per
-// stage, else the present offsets taken SEGS at a time.
-template <int CS, int SEGS>
+// Stages of a unit.  Block stages (GRP false): each present offset's cin/64
+// channel blocks, SEGS consecutive blocks per stage.  Group stages (GRP
+// true, cin == CS): the present offsets taken SEGS at a time.
+template <int CS, int SEGS, bool GRP>
 __device__ __forceinline__ int unit_stages(uint32_t mask, int cin) {
   const int np = __popc(mask);
-  if constexpr (SEGS == 1) {
-    return np * (cin >> 6);
+  if constexpr (!GRP) {
+    return np * (cin >> 6) / SEGS;
   } else {
     return (np + SEGS - 1) / SEGS;
   }
 }
 
-// Walks the K slices of a unit in order: with one segment per stage, each
-// present offset k (ascending) with its cin/64 channel blocks; otherwise the
-// present offsets SEGS at a time (k = taps, one past the last offset, pads
-// the last stage: its W box lies past the end of W and is zero-filled).
-// next() fills the stage's offsets and returns its first channel.
-template <int CS, int SEGS>
+// Walks the K slices of a unit in order.  Block stages: each present offset
+// k (ascending) with its cin/64 channel blocks, SEGS blocks per stage (all
+// segments of a stage take offset k; segment j starts at channel c0 + 64 j).
+// Group stages: the present offsets SEGS at a time (k = taps, one past the
+// last offset, pads the last stage: its W box lies past the end of W and is
+// zero-filled).  next() fills the stage's offsets and returns its first
+// channel.
+template <int CS, int SEGS, bool GRP>
 struct OffsetIter {
   uint32_t rem;
   int cblk = 0, cblocks, taps;
@@ -279,8 +282,8 @@ struct OffsetIter {
       : rem(mask), cblocks(cin >> 6), taps(taps_) {}
   // Step over the first `n` stages.
   __device__ __forceinline__ void skip(int n) {
-    if constexpr (SEGS == 1) {
-      cblk += n;
+    if constexpr (!GRP) {
+      cblk += n * SEGS;
       while (cblk >= cblocks) {
         cblk -= cblocks;
         rem &= rem - 1u;
@@ -290,10 +293,13 @@ struct OffsetIter {
     }
   }
   __device__ __forceinline__ int next(int (&ks)[SEGS]) {
-    if constexpr (SEGS == 1) {
-      ks[0] = __ffs(rem) - 1;
+    if constexpr (!GRP) {
+      const int k = __ffs(rem) - 1;
+#pragma unroll
+      for (int j = 0; j < SEGS; ++j) ks[j] = k;
       const int c0 = cblk * 64;
-      if (++cblk == cblocks) {
+      cblk += SEGS;
+      if (cblk == cblocks) {
         cblk = 0;
         rem &= rem - 1u;
       }
@@ -336,7 +342,7 @@ __global__ void __launch_bounds__(256) k_zero_rows_of(float4* __restrict__ out,
 
 // FUSED: the epilogue applies an activation, adds a residual or rounds to
 // bf16 (the plain variant only adds the bias and stores fp32).
-template <int NPAD, int CS, int SEGS, int CL, bool FUSED>
+template <int NPAD, int CS, int SEGS, bool GRP, int CL, bool FUSED>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_conv_tc(const __grid_constant__ CUtensorMap tm_b, const TcArgs p) {
   using C = TcCfg<NPAD, CS, SEGS>;
@@ -425,14 +431,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         have_next = ahead.next(p, ncl, wn);  // the item after wi
         const uint32_t mask = unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles);
         int s0, s1;
-        item_range(wi, p.sv, unit_stages<CS, SEGS>(mask, p.cin), s0, s1);
+        item_range(wi, p.sv, unit_stages<CS, SEGS, GRP>(mask, p.cin), s0, s1);
         if constexpr (C::kNbrBufs == 2) {
           if (!issue_nbr(have_next, wn, buf ^ 1)) {
             ok = false;
             break;
           }
         }
-        OffsetIter<CS, SEGS> it(mask, p.cin, p.taps);
+        OffsetIter<CS, SEGS, GRP> it(mask, p.cin, p.taps);
         it.skip(s0);
         for (int s = s0; s < s1; ++s) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
@@ -453,7 +459,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               if ((uint32_t)(b % CL) == rank) {
                 // k == 27 addresses rows past W's end: the box is zero-filled.
                 uint8_t* dst = b_st + nb2 * (C::kKst * 128) + j * CS * 128;
-                const int32_t y = ks[j] * p.cin + c0;
+                const int32_t y = ks[j] * p.cin + c0 + (GRP ? 0 : 64 * j);
                 if constexpr (CL > 1)
                   tma_load_2d_multicast(dst, &tm_b, &full[stage], nb2 * 64, y, kAllCtas);
                 else
@@ -532,7 +538,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool has_rows = tile < p.ntiles;
       const uint32_t mask = unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles);
       int s0, s1;
-      item_range(wi, p.sv, unit_stages<CS, SEGS>(mask, p.cin), s0, s1);
+      item_range(wi, p.sv, unit_stages<CS, SEGS, GRP>(mask, p.cin), s0, s1);
       if (has_rows) {
         if (!mbar_wait_bounded(&nbr_full[buf], (nbr_phase >> buf) & 1u, abort_flag)) {
           ok = false;
@@ -541,7 +547,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         nbr_phase ^= 1u << buf;
       }
       const int32_t* nb = s_nbr + buf * (kTileRows * kTaps);
-      OffsetIter<CS, SEGS> it(mask, p.cin, p.taps);
+      OffsetIter<CS, SEGS, GRP> it(mask, p.cin, p.taps);
       it.skip(s0);
       for (int s = s0; s < s1; ++s, ++gst) {
         int ks[C::kSegs];
@@ -577,9 +583,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (kb[j] < 0) row[i] = -1;
         }
 #pragma unroll
-        for (int i = 0; i < C::kPerThread; ++i)
-          cp_async_16(a_st + dst_i[i], row[i] >= 0 ? fsrc + (int64_t)row[i] * rstride : fbase,
+        for (int i = 0; i < C::kPerThread; ++i) {
+          // Block stages: segment j is the next 64-channel block of the row.
+          const int j = i * C::kGroupThreads / C::kSegCopies;
+          const char* const fseg = fsrc + (GRP ? 0 : j * 128);
+          cp_async_16(a_st + dst_i[i], row[i] >= 0 ? fseg + (int64_t)row[i] * rstride : fbase,
                       row[i] >= 0 ? 16u : 0u);
+        }
         cp_async_arrive_noinc(&full[stage]);
         if (++stage == C::kStages) {
           stage = 0;
@@ -608,7 +618,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       WorkItem wi;
       while (ok && items.next(p, ncl, wi)) {
         int s0, s1;
-        item_range(wi, p.sv, unit_stages<CS, SEGS>(unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles), p.cin),
+        item_range(wi, p.sv, unit_stages<CS, SEGS, GRP>(unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles), p.cin),
                    s0, s1);
         if (s0 == s1) continue;  // an empty part: no accumulator, no epilogue
         const int nst = s1 - s0;
@@ -678,7 +688,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (add) {
         int s0, s1;
         item_range(wi, p.sv,
-                   unit_stages<CS, SEGS>(unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles), p.cin), s0, s1);
+                   unit_stages<CS, SEGS, GRP>(unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles), p.cin), s0, s1);
         if (s0 == s1) continue;
       }
       const float bscale = last ? 1.f : 0.f;
@@ -945,11 +955,11 @@ int tail_split(int64_t nunits, int64_t G, int max_stages) {
   return best_t < 0.95 * t1 ? best : 1;
 }
 
-template <int NPAD, int CS, int SEGS, int CL, bool FUSED>
+template <int NPAD, int CS, int SEGS, bool GRP, int CL, bool FUSED>
 cudaError_t launch_typed(const ConvMap& m, const void* feats, const void* w, bool f16,
                          const Epilogue& ep, int cin, int cout, cudaStream_t s) {
   using C = TcCfg<NPAD, CS, SEGS>;
-  auto kern = k_conv_tc<NPAD, CS, SEGS, CL, FUSED>;
+  auto kern = k_conv_tc<NPAD, CS, SEGS, GRP, CL, FUSED>;
   static LaunchCache cache;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1014,7 +1024,7 @@ cudaError_t launch_typed(const ConvMap& m, const void* feats, const void* w, boo
   a.cout = cout;
   const int64_t nunits = (m.ntiles + CL - 1) / CL;
   if (nunits == 0) return cudaSuccess;
-  const int max_stages = SEGS == 1 ? m.taps * (cin / 64) : (m.taps + SEGS - 1) / SEGS;
+  const int max_stages = !GRP ? m.taps * (cin / 64) / SEGS : (m.taps + SEGS - 1) / SEGS;
   // An activation or a 16-bit output cannot be applied to partial sums.  In
   // place (residual == out), the split rows would be zeroed, and other parts'
   // sums added, before the last part reads the residual from them.
@@ -1050,20 +1060,20 @@ cudaError_t launch_typed(const ConvMap& m, const void* feats, const void* w, boo
   return e;
 }
 
-template <int NPAD, int CS, int SEGS>
+template <int NPAD, int CS, int SEGS, bool GRP>
 cudaError_t launch_cl(const ConvMap& m, const void* feats, const void* w, bool f16,
                       const Epilogue& ep, int cin, int cout, cudaStream_t s) {
   const bool fused = ep.act || ep.residual || ep.out_half;
   if constexpr (NPAD >= 256) {
     if (cluster_size(NPAD) == 4)
-      return fused ? launch_typed<NPAD, CS, SEGS, 4, true>(m, feats, w, f16, ep, cin, cout, s)
-                   : launch_typed<NPAD, CS, SEGS, 4, false>(m, feats, w, f16, ep, cin, cout, s);
+      return fused ? launch_typed<NPAD, CS, SEGS, GRP, 4, true>(m, feats, w, f16, ep, cin, cout, s)
+                   : launch_typed<NPAD, CS, SEGS, GRP, 4, false>(m, feats, w, f16, ep, cin, cout, s);
   }
   if (cluster_size(NPAD) == 2)
-    return fused ? launch_typed<NPAD, CS, SEGS, 2, true>(m, feats, w, f16, ep, cin, cout, s)
-                 : launch_typed<NPAD, CS, SEGS, 2, false>(m, feats, w, f16, ep, cin, cout, s);
-  return fused ? launch_typed<NPAD, CS, SEGS, 1, true>(m, feats, w, f16, ep, cin, cout, s)
-               : launch_typed<NPAD, CS, SEGS, 1, false>(m, feats, w, f16, ep, cin, cout, s);
+    return fused ? launch_typed<NPAD, CS, SEGS, GRP, 2, true>(m, feats, w, f16, ep, cin, cout, s)
+                 : launch_typed<NPAD, CS, SEGS, GRP, 2, false>(m, feats, w, f16, ep, cin, cout, s);
+  return fused ? launch_typed<NPAD, CS, SEGS, GRP, 1, true>(m, feats, w, f16, ep, cin, cout, s)
+               : launch_typed<NPAD, CS, SEGS, GRP, 1, false>(m, feats, w, f16, ep, cin, cout, s);
 }
 
 // Wide stages for narrow layers (build-time SC_NARROW_K128, default on).
@@ -1071,6 +1081,12 @@ cudaError_t launch_cl(const ConvMap& m, const void* feats, const void* w, bool f
 #define SC_NARROW_K128 1
 #endif
 constexpr bool kNarrowStages = SC_NARROW_K128 != 0;
+// Two-block stages for wide inputs with cout <= 128 (build-time
+// SC_WIDE_K128, default on).
+#ifndef SC_WIDE_K128
+#define SC_WIDE_K128 1
+#endif
+constexpr bool kWideStages = SC_WIDE_K128 != 0;
 
 template <int NPAD>
 cudaError_t launch_npad(const ConvMap& m, const void* feats, const void* w, bool f16,
@@ -1078,10 +1094,19 @@ cudaError_t launch_npad(const ConvMap& m, const void* feats, const void* w, bool
   // Narrow layers (cout <= 64, cin <= 64): K = 128 per stage, so that each
   // stage's fixed synchronisation cost is spread over eight MMAs.
   constexpr int W = (NPAD <= 64 && kNarrowStages) ? 2 : 1;
-  if (cin == 16) return launch_cl<NPAD, 16, 4 * W>(m, feats, w, f16, ep, cin, cout, s);
-  if (cin == 32) return launch_cl<NPAD, 32, 2 * W>(m, feats, w, f16, ep, cin, cout, s);
-  if (cin == 64) return launch_cl<NPAD, 64, W>(m, feats, w, f16, ep, cin, cout, s);
-  return launch_cl<NPAD, 64, 1>(m, feats, w, f16, ep, cin, cout, s);
+  if (cin == 16) return launch_cl<NPAD, 16, 4 * W, true>(m, feats, w, f16, ep, cin, cout, s);
+  if (cin == 32) return launch_cl<NPAD, 32, 2 * W, true>(m, feats, w, f16, ep, cin, cout, s);
+  if (cin == 64) {
+    if constexpr (W == 2) return launch_cl<NPAD, 64, 2, true>(m, feats, w, f16, ep, cin, cout, s);
+    return launch_cl<NPAD, 64, 1, false>(m, feats, w, f16, ep, cin, cout, s);
+  }
+  // Wide inputs with cout <= 128: two 64-channel blocks of an offset per
+  // stage (K = 128), where the blocks pair up.
+  if constexpr (NPAD <= 128 && kWideStages) {
+    if ((cin / 64) % 2 == 0)
+      return launch_cl<NPAD, 64, 2, false>(m, feats, w, f16, ep, cin, cout, s);
+  }
+  return launch_cl<NPAD, 64, 1, false>(m, feats, w, f16, ep, cin, cout, s);
 }
 
 }  // namespace
