@@ -100,8 +100,12 @@ constexpr int kProducerThreads = 32 * kProducerWarps;
 #define SC_PRODUCER_GROUPS 0
 #endif
 template <int NPAD>
-constexpr int producer_groups(int stages) {
-  return SC_PRODUCER_GROUPS > 0 ? SC_PRODUCER_GROUPS : (NPAD <= 64 && stages >= 4 ? 4 : 2);
+constexpr int producer_groups(int stages, int stage_copies) {
+  // Four groups only where each thread's share of a stage stays at 16
+  // copies or fewer (its per-copy registers), two otherwise.
+  return SC_PRODUCER_GROUPS > 0
+             ? SC_PRODUCER_GROUPS
+             : (NPAD <= 64 && stages >= 4 && stage_copies <= 16 * (kProducerThreads / 4) ? 4 : 2);
 }
 constexpr int kMmaWarp = 5 + kProducerWarps;
 constexpr int kTcThreads = 32 * (kMmaWarp + 1);
@@ -136,7 +140,13 @@ struct TcCfg {
   static constexpr int kSegCopies = kTileRows * kChunks;        // 16-byte copies per segment
   static constexpr int kASeg = kTileRows * kRowBytes;   // bytes per A segment
   static constexpr int kABytes = kTileRows * kKst * 2;  // 16 or 32 KB per stage
-  static constexpr int kBlocksN = NPAD / 64;            // 64-column blocks of B
+  // B blocks: 64 columns (128-byte rows, 128-byte swizzle), or all of a
+  // 32-column B (64-byte rows, 64-byte swizzle).
+  static constexpr int kBCols = NPAD < 64 ? NPAD : 64;  // columns per B block
+  static constexpr int kBRow = kBCols * 2;              // bytes per K row of a block
+  static constexpr int kBlocksN = NPAD / kBCols;        // column blocks of B
+  static constexpr uint32_t kLayoutB = kBRow == 128 ? 2u : 4u;
+  static_assert(kBRow == 128 || kBRow == 64, "B blocks of 64 or 32 columns");
   static constexpr int kBBytes = kKst * NPAD * 2;       // kKst K rows x NPAD bf16
   static constexpr int kStageBytes = kABytes + kBBytes;
   // Neighbour blocks: two (the next unit's prefetched during this one) for
@@ -149,7 +159,7 @@ struct TcCfg {
   static constexpr int kStages0 = (kSmemLimit - 1024 - kFixed) / kStageBytes;
   static constexpr int kStages = kStages0 > SC_MAX_STAGES ? SC_MAX_STAGES : kStages0;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kFixed;
-  static constexpr int kGroups = producer_groups<NPAD>(kStages);
+  static constexpr int kGroups = producer_groups<NPAD>(kStages, kSegs * kSegCopies);
   static constexpr int kGroupThreads = kProducerThreads / kGroups;
   static_assert(kGroupThreads * kGroups == kProducerThreads && kGroupThreads % 32 == 0,
                 "producer groups are whole warps");
@@ -458,12 +468,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const int b = j * C::kBlocksN + nb2;
               if ((uint32_t)(b % CL) == rank) {
                 // k == 27 addresses rows past W's end: the box is zero-filled.
-                uint8_t* dst = b_st + nb2 * (C::kKst * 128) + j * CS * 128;
+                uint8_t* dst = b_st + nb2 * (C::kKst * C::kBRow) + j * CS * C::kBRow;
                 const int32_t y = ks[j] * p.cin + c0 + (GRP ? 0 : 64 * j);
                 if constexpr (CL > 1)
-                  tma_load_2d_multicast(dst, &tm_b, &full[stage], nb2 * 64, y, kAllCtas);
+                  tma_load_2d_multicast(dst, &tm_b, &full[stage], nb2 * C::kBCols, y, kAllCtas);
                 else
-                  tma_load_2d(dst, &tm_b, &full[stage], nb2 * 64, y);
+                  tma_load_2d(dst, &tm_b, &full[stage], nb2 * C::kBCols, y);
               }
             }
           }
@@ -613,7 +623,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = true;
       // Operand descriptors of stage 0, segment 0, K step 0.
       const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, C::kSboA, C::kLayoutA);
-      const uint64_t b_desc0 = smem_desc(smem_u32(sB), C::kKst * 128, 1024, 2u);
+      const uint64_t b_desc0 = smem_desc(smem_u32(sB), C::kKst * C::kBRow, 8 * C::kBRow, C::kLayoutB);
       ItemIter items(p, cid);
       WorkItem wi;
       while (ok && items.next(p, ncl, wi)) {
@@ -645,7 +655,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < CS / 16; ++kk) {
               const uint64_t ad = ad_s + (uint64_t)((j * C::kASeg + kk * 32) >> 4);
-              const uint64_t bd = bd_s + (uint64_t)(((j * CS + kk * 16) * 128) >> 4);
+              const uint64_t bd = bd_s + (uint64_t)(((j * CS + kk * 16) * C::kBRow) >> 4);
               tc_mma_bf16(d_tmem, ad, bd, p.idesc, (s | j | kk) != 0 ? 1u : 0u);
             }
           }
@@ -1001,8 +1011,8 @@ cudaError_t launch_typed(const ConvMap& m, const void* feats, const void* w, boo
   }
 
   alignas(64) CUtensorMap tm_b;
-  if (!encode_2d(&tm_b, w, (uint64_t)cout, (uint64_t)m.taps * cin, (uint64_t)cout * 2, 64, CS,
-                 CU_TENSOR_MAP_SWIZZLE_128B,
+  if (!encode_2d(&tm_b, w, (uint64_t)cout, (uint64_t)m.taps * cin, (uint64_t)cout * 2, C::kBCols,
+                 CS, C::kBRow == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                  f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
     return cudaErrorInvalidValue;
   TcArgs a;
@@ -1122,8 +1132,12 @@ bool conv_tc_supported(int cin, int cout) {
 cudaError_t launch_conv_tc(const ConvMap& m, const void* feats, const void* w, bool f16,
                            const Epilogue& ep, int cin, int cout, cudaStream_t s) {
   if (!conv_tc_supported(cin, cout)) return cudaErrorNotSupported;
-  const int npad = (cout + 63) / 64 * 64;
+  // cout <= 32 runs as N = 32 (an M = 128 MMA takes N in steps of 16; the
+  // narrower B halves the shared-memory bytes of W per stage), otherwise
+  // cout rounded up to 64.
+  const int npad = cout <= 32 ? 32 : (cout + 63) / 64 * 64;
   switch (npad) {
+    case 32: return launch_npad<32>(m, feats, w, f16, ep, cin, cout, s);
     case 64: return launch_npad<64>(m, feats, w, f16, ep, cin, cout, s);
     case 128: return launch_npad<128>(m, feats, w, f16, ep, cin, cout, s);
     case 192: return launch_npad<192>(m, feats, w, f16, ep, cin, cout, s);
