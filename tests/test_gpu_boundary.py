@@ -187,7 +187,7 @@ def test_probe_limit_reports_table_full(sc):
 # ---------------------------------------------------------------------------
 # asynchronous build
 
-@pytest.mark.parametrize("key", [2, 3, 5])
+@pytest.mark.parametrize("key", [1, 2, 3, 4, 5])
 def test_async_build_matches_oracle(sc, key):
     p = synth.make_problem(key)
     coords = dev(p.coords)
@@ -198,6 +198,28 @@ def test_async_build_matches_oracle(sc, key):
     np.testing.assert_array_equal(table(sc, m), want)
     sc.sc_map_status(m)
     assert m.pairs == int((want >= 0).sum())
+    m.free()
+
+
+@pytest.mark.parametrize("res,nbatch,density", [(1, 3, 1.0), (2, 2, 0.7), (33, 4, 0.2),
+                                               (31, 1, 0.5), (64, 6, 0.05)])
+def test_async_build_small_and_odd_grids(sc, res, nbatch, density):
+    """Asynchronous builds on small and odd grids: cells on the grid's faces,
+    res 1 and 2, res not a multiple of 32, an empty batch element, unused
+    batch indices below nbatch and shuffled rows: the map equals the
+    oracle's."""
+    rng = np.random.default_rng(res * 100 + nbatch)
+    rows = []
+    for b in range(nbatch):
+        if nbatch > 2 and b == 1:
+            continue                                   # an empty batch element
+        xyz = np.argwhere(rng.random((res, res, res)) < density)
+        rows.append(np.concatenate([np.full((len(xyz), 1), b), xyz], axis=1))
+    c = np.concatenate(rows).astype(np.int32)
+    c = np.ascontiguousarray(c[rng.permutation(len(c))])
+    m = sc.sc_build_map_async(dev(c), res, nbatch + 1)
+    np.testing.assert_array_equal(table(sc, m), oracle.build_neighbor_table(c, res))
+    sc.sc_map_status(m)
     m.free()
 
 
