@@ -228,7 +228,7 @@ def test_conv_configs_sampled(sc, key):
 
 
 SHAPES = [(16, 16), (32, 48), (64, 64), (64, 192), (128, 32), (192, 256), (256, 256),
-          (1024, 16), (32, 256)]
+          (1024, 16), (32, 256), (128, 128), (256, 96), (512, 64)]
 
 
 @pytest.mark.parametrize("cin,cout", SHAPES)
@@ -468,6 +468,33 @@ def test_fused_epilogue_split_shapes(sc, act, odt):
     acts = {"none": oracle.ACT_NONE, "relu": oracle.ACT_RELU, "silu": oracle.ACT_SILU}
     ref = oracle.epilogue(oracle.conv(want[rows], p.feats, p.weight, p.bias), acts[act], r[rows])
     check_epilogue_out(got[rows], ref, odt, "bf16", "split %s %s" % (act, odt))
+
+
+@pytest.mark.parametrize("cin,cout", [(32, 32), (16, 16), (128, 32), (128, 128), (256, 64)])
+@pytest.mark.parametrize("act,odt,resid", [("silu", "bf16", True), ("relu", "f32", True),
+                                           ("none", "f16", False)])
+def test_fused_epilogue_stage_shapes(sc, cin, cout, act, odt, resid):
+    """The fused epilogue on every stage layout: N = 32 outputs (cout <= 32),
+    several offsets per stage (cin <= 64), two 64-channel blocks of one
+    offset per stage (cin a multiple of 128, cout <= 128, with and without the
+    CTA-pair W multicast), against the oracle's map and convolution."""
+    rng = np.random.default_rng(cin * 7 + cout)
+    coords = random_coords(rng, 2, 14, 0.25)          # ~1370 rows: 11 tiles, ragged tail
+    feats, weight, bias = synth.make_tensors(len(coords), cin, cout, "bf16", cin + cout + 5)
+    tout = TORCH_DT[odt]
+    r = _residual(len(coords), cout, odt, cin + cout) if resid else None
+    m, nbr = gpu_map(sc, coords, 14)
+    want = oracle.build_neighbor_table(coords, 14)
+    np.testing.assert_array_equal(nbr, want)
+    out = sc.sc_forward_ex(m, to_dev(feats, torch.bfloat16), to_dev(weight, torch.bfloat16),
+                           to_dev(bias), residual=None if r is None else to_dev(r, tout),
+                           act=act, out_dtype=tout)
+    sc.sc_device_status(m)
+    got = out.float().cpu().numpy().astype(np.float64)
+    m.free()
+    acts = {"none": oracle.ACT_NONE, "relu": oracle.ACT_RELU, "silu": oracle.ACT_SILU}
+    ref = oracle.epilogue(oracle.conv(want, feats, weight, bias), acts[act], r)
+    check_epilogue_out(got, ref, odt, "bf16", "%dx%d %s %s" % (cin, cout, act, odt))
 
 
 @pytest.mark.parametrize("odt", ["f32", "bf16"])
