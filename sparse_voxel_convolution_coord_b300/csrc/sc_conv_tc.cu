@@ -17,9 +17,11 @@
 // present in the tile (its 27-bit OR mask), the 128 neighbour rows are
 // gathered straight from the feature matrix by cp.async (absent neighbours
 // zero-filled) and W[k] arrives by tiled TMA; a single thread issues
-// tcgen05.mma (M = 128, N = cout padded to 64, K = 16, bf16 x bf16 or fp16 x
-// fp16 -> fp32; the instruction descriptor is a launch argument) into a TMEM
-// accumulator.  Each output row belongs to exactly one tile, so the epilogue
+// tcgen05.mma (M = 128, N = cout padded to 64, or 32 when cout <= 32, K = 16,
+// bf16 x bf16 or fp16 x fp16 -> fp32; the instruction descriptor is a launch
+// argument) into a TMEM accumulator.  A pipeline stage holds K = 64 or 128
+// channels: one offset's 64-channel block (or two, for wide inputs with
+// cout <= 128), or the whole rows of several offsets (cin <= 64).  Each output row belongs to exactly one tile, so the epilogue
 // (TMEM -> registers -> shared staging -> coalesced stores) needs no atomics,
 // except in the tail split below.
 //
@@ -50,12 +52,13 @@
 //              (two buffers, one unit ahead, for cout <= 64; one buffer,
 //              refilled after a unit's stages, above) and, per stage, this
 //              CTA's W boxes by tiled TMA
-//   warps 5-12 A producers: per pipeline stage the 256 threads gather the
-//              A rows with 16-byte cp.async copies (consecutive threads take
-//              consecutive 16-byte chunks of a row, so a warp instruction
-//              moves whole lines; absent neighbours are zero-filled) straight
-//              into the swizzled operand layout; each thread's mbarrier
-//              arrival fires when its copies land.  (TMA gather4 moves only
+//   warps 5-12 A producers, in 2 or 4 groups that take the stages in turn:
+//              per stage the group's threads gather the A rows with 16-byte
+//              cp.async copies (consecutive threads take consecutive 16-byte
+//              chunks of a row, so a warp instruction moves whole lines;
+//              absent neighbours are zero-filled) straight into the swizzled
+//              operand layout; each thread's mbarrier arrival fires when its
+//              copies land.  (TMA gather4 moves only
 //              four 64-128 byte rows per operation; its per-operation cost,
 //              not bandwidth, bounded the gather.)
 //   warp 13    TMEM allocation; lane 0 issues the MMAs and the commits
@@ -65,12 +68,13 @@
 //
 // Shared-memory operand layouts (A written swizzled by the producers'
 // cp.async addresses, B by TMA swizzling):
-//   A (gathered rows, K-major): per stage 64/CS segments, each 128 rows x CS
+//   A (gathered rows, K-major): per stage SEGS segments, each 128 rows x CS
 //     16-bit values, rows of 2*CS bytes with the matching 128/64/32-byte
 //     swizzle;
-//   B (W[k] rows, MN-major): per stage [cout/64 blocks][64 K rows][128 B],
-//     128-byte swizzle; LBO = 8 KB between 64-column blocks, SBO = 1 KB
-//     between 8-row groups.
+//   B (W[k] rows, MN-major): per stage [column blocks][K rows][128 B] with
+//     the 128-byte swizzle (64-column blocks; LBO = K x 128 B between
+//     blocks, SBO = 1 KB between 8-row groups), or [K rows][64 B] with the
+//     64-byte swizzle at N = 32 (SBO = 512 B).
 #include <algorithm>
 #include <atomic>
 #include <cstdlib>
