@@ -443,6 +443,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ok = issue_nbr(have_next, wn, 0);
       while (ok && items.next(p, ncl, wi)) {
         have_next = ahead.next(p, ncl, wn);  // the item after wi
+        if constexpr (C::kNbrBufs == 1) {
+          // One buffer: the next unit's block is copied in only once this
+          // unit's gathers are issued; bring it into L2 now, so that the
+          // copy then does not wait on DRAM.
+          const int64_t tn = wn.unit * CL + rank;
+          if (have_next && tn < p.ntiles)
+            bulk_prefetch_l2(p.nbr + tn * (kTileRows * p.taps), (uint32_t)(p.taps * kTileRows * 4));
+        }
         const uint32_t mask = unit_mask<CL>(p.tile_mask, wi.unit, p.ntiles);
         int s0, s1;
         item_range(wi, p.sv, unit_stages<CS, SEGS, GRP>(mask, p.cin), s0, s1);
