@@ -273,8 +273,8 @@ def run_reference(args):
 # valid only for the kernel source it was measured on (sha1 of the file).
 MEASURED_TRAFFIC = {
     # workload name: (sha1 of sc_conv_tc.cu, bytes per launch)
-    "sq3x64_30k_c256_bf16": ("fb556aeb3b9e67d2f5bb48a8647c3b5b185ce58a", 33275136 + 20736),
-    "sq4x256_400k_c32_bf16": ("fb556aeb3b9e67d2f5bb48a8647c3b5b185ce58a", 68204032 + 13150720),
+    "sq3x64_30k_c256_bf16": ("8332b9567355d28652c63bb7c941e7161598393a", 33275648 + 51712),
+    "sq4x256_400k_c32_bf16": ("8332b9567355d28652c63bb7c941e7161598393a", 68204288 + 13037056),
 }
 
 
