@@ -29,7 +29,8 @@
 //                    consecutive rows of one offset).  Each block ORs its
 //                    rows' presence bits into the tile mask the convolution
 //                    uses to skip absent offsets, and adds its pair count to
-//                    one of 32 global counters.  Used up to 2^20 voxels.
+//                    one of 32 global counters.  Used up to 2^20 voxels;
+//                    from 2^18 voxels each thread takes three columns.
 //  k_neighbor_query32  (32-bit keys, 2^20 voxels and more) one thread per
 //                    voxel: the 27 cells around it fall in 2 x 2 x 2 bricks
 //                    whose group hashes follow from one by additions, so all
@@ -577,8 +578,18 @@ cudaError_t launch_neighbor_query(const int32_t* coords, const HashParams& hp, i
     // 30k-voxel build, 49 against 54 us at 400k); beyond, the kernel with
     // one thread per voxel and all 26 loads in flight is faster (386 against
     // 457 us at 3.3M).
+    // From 2^18 voxels three columns per thread (fewer threads, their setup
+    // shared) beat one (measured: 46.1 against 48.1 us at 400k; 17.3 against
+    // 15.3 us at 30k and 25.5 against 23.5 us at 144k the other way).
     cudaError_t e;
-    if (hp.n < (int64_t(1) << 20)) {
+    if (kQueryCols == 1 && hp.n >= (int64_t(1) << 18) && hp.n < (int64_t(1) << 20)) {
+      const dim3 grid((unsigned)tiles, 3);
+      e = layout == kNbrTileMajor
+              ? launch_dependent2(k_neighbor_query<kNbrTileMajor, true, 3>, grid, kTileRows, s,
+                                  c4, hp, nbr, tile_mask, pair_count)
+              : launch_dependent2(k_neighbor_query<kNbrRowMajor, true, 3>, grid, kTileRows, s,
+                                  c4, hp, nbr, tile_mask, pair_count);
+    } else if (hp.n < (int64_t(1) << 20)) {
       const dim3 grid((unsigned)tiles, 9 / kQueryCols);
       e = layout == kNbrTileMajor
               ? launch_dependent2(k_neighbor_query<kNbrTileMajor, true, kQueryCols>, grid,
