@@ -231,9 +231,12 @@ struct ItemIter {
     if (k >= p.nparts) {
       w = {k - p.nparts, 0, p.sv};
     } else {
-      const int part = (int)(k / p.tail);
-      w = {p.whole + k % p.tail, (int)((int64_t)part * p.sv / p.split),
-           (int)((int64_t)(part + 1) * p.sv / p.split)};
+      // k < nparts = tail x split and part < split <= 8: 32-bit arithmetic.
+      const uint32_t kk = (uint32_t)k, tail = (uint32_t)p.tail;
+      const int part = (int)(kk / tail);
+      w = {p.whole + (int64_t)(kk - (uint32_t)part * tail),
+           (int)((uint32_t)(part * p.sv) / (uint32_t)p.split),
+           (int)((uint32_t)((part + 1) * p.sv) / (uint32_t)p.split)};
     }
     k += ncl;
     return true;
@@ -242,8 +245,15 @@ struct ItemIter {
 
 // Stage range [s0, s1) of an item of a unit with nst stages.
 __device__ __forceinline__ void item_range(const WorkItem& w, int sv, int nst, int& s0, int& s1) {
-  s0 = (int)((int64_t)w.a * nst / sv);
-  s1 = (int)((int64_t)w.b * nst / sv);
+  if (w.a == 0 && w.b == sv) {  // a whole unit
+    s0 = 0;
+    s1 = nst;
+    return;
+  }
+  // a, b <= sv and nst <= sv, with sv at most taps x (1024 / 64): 32 bits hold
+  // the products.
+  s0 = (int)((uint32_t)(w.a * nst) / (uint32_t)sv);
+  s1 = (int)((uint32_t)(w.b * nst) / (uint32_t)sv);
 }
 
 // Bounded wait with its own limit; ignores the abort flag (used to drain).
