@@ -273,8 +273,8 @@ def run_reference(args):
 # valid only for the kernel source it was measured on (sha1 of the file).
 MEASURED_TRAFFIC = {
     # workload name: (sha1 of sc_conv_tc.cu, bytes per launch)
-    "sq3x64_30k_c256_bf16": ("c961fb58228d22a6bdf1501b8b1c72f0190ed5ed", 33265920 + 23808),
-    "sq4x256_400k_c32_bf16": ("c961fb58228d22a6bdf1501b8b1c72f0190ed5ed", 68197120 + 13501696),
+    "sq3x64_30k_c256_bf16": ("c673aed9615fe250034075d9bc52bd3538000c69", 33265664 + 27392),
+    "sq4x256_400k_c32_bf16": ("c673aed9615fe250034075d9bc52bd3538000c69", 68185088 + 13070592),
 }
 
 

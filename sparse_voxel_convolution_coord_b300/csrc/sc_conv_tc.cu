@@ -350,17 +350,20 @@ __global__ void __launch_bounds__(256) k_zero_rows(float4* __restrict__ p, int64
 }
 
 // The same for the rows of positions [pos0, n) through a row indirection
-// (c4 = cout / 4 float4 per row).
+// (c4 = cout / 4 float4 per row): a warp per position, its lanes over the
+// row's float4 columns.
 __global__ void __launch_bounds__(256) k_zero_rows_of(float4* __restrict__ out,
                                                       const int32_t* __restrict__ row_of,
                                                       int64_t pos0, int64_t n, int c4) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int64_t total = (n - pos0) * c4;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-    const int64_t pos = pos0 + i / c4;
+  const int lane = threadIdx.x & 31;
+  const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t pos = pos0 + (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); pos < n;
+       pos += wstride) {
     const int32_t row = __ldg(row_of + pos);
-    if (row >= 0) out[(int64_t)row * c4 + i % c4] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row < 0) continue;
+    float4* dst = out + (int64_t)row * c4;
+    for (int c = lane; c < c4; c += 32) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
